@@ -1,0 +1,257 @@
+/*
+ * hs.h — C ABI of the GB300 (sm_103a) sparse-MLA (DeepSeek sparse attention, "DSA") hot path.
+ *
+ * Four calls make one attention layer's data-parallel hot path:
+ *
+ *   hs_indexer_scores   lightning-indexer scores of every visible prior token  (FP8 tcgen05 GEMM)
+ *   hs_topk             per-query top-k of those scores, lowest index wins ties
+ *   hs_sparse_mla_fwd   softmax attention of all heads over the selected latent-KV rows
+ *   hs_hisparse_resolve serve each selected token from resident KV, the hot buffer (LRU),
+ *                       or a copy from pinned host memory into an LRU slot
+ *
+ * Sources (web pages describing GLM-5.x serving with DSA in vLLM):
+ *   [P1] "vLLM v0.32.0 GLM-5.3 サービング: 16基のH200上でのPCP、DCP、およびハイブリッドHiSparse"
+ *   [P2] "Optimizaciones de GLM-5.3, Parte 2: PCP, DCP e Hybrid HiSparse en 16 H200"
+ *   [P3] "vLLM GLM 5.3 最適化: ハイブリッド HiSparse オフロード"
+ *   [P4] "vLLMによるNVIDIA B300 GPU上でのGLM-5.2のサービング"
+ *
+ * Conventions shared by every call
+ *  - All buffers are caller-owned device memory unless stated; the library allocates nothing
+ *    and keeps no state between calls (hs_last_error's thread-local string aside).
+ *  - Every call only enqueues work on `stream` (NULL = legacy default stream); none waits on
+ *    the host for the GPU.
+ *  - Arguments are checked on the host first. A bad argument returns HS_ERR_INVALID and
+ *    launches nothing; hs_last_error() then names the argument.
+ *  - Data that only the GPU sees (indices, lengths, block-table entries) is checked in the
+ *    kernels. A bad value sets a bit of *err_flag (an int32 in device memory that the caller
+ *    zeroes and reads whenever it likes) and the offending element is skipped. Kernels never
+ *    trap. Every wait inside a kernel is bounded; running out sets HS_FLAG_TIMEOUT.
+ *  - Requires a device of compute capability 10.3 (sm_103a); otherwise HS_ERR_UNSUPPORTED.
+ *
+ * Layouts
+ *  - FP8 is OCP e4m3 ("e4m3fn": bias 7, no infinities, 0x7F/0xFF are NaN).
+ *  - Paged KV: pages of HS_PAGE = 64 tokens. A request's token j lives in physical page
+ *    block_table[r * bt_stride + j / 64], at row (page * 64 + j % 64) of the pool.
+ *  - Latent-KV row ("fp8_ds_mla", 656 bytes, [P1] section 「数字がうまくいく理由」: 656 B of FP8 KV
+ *    plus a 4 B index per gathered row):
+ *        bytes   0..511  512 x e4m3 latent codes
+ *        bytes 512..527  4 x fp32 dequantisation scales, one per 128-element group
+ *        bytes 528..655  64 x bf16 RoPE part, used as stored
+ *    latent[c] = e4m3(code[c]) * scale[c / 128].
+ *  - Indexer key row: Di e4m3 codes in k_cache plus one fp32 scale in k_scale
+ *    ([P1] same section: 128 FP8 values and a 4-byte scale).
+ */
+#ifndef HS_H_
+#define HS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as CUDA's cudaStream_t, declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* hs_stream_t;
+
+typedef enum {
+  HS_OK = 0,
+  HS_ERR_INVALID = 1,      /* an argument failed the host-side checks; nothing was launched */
+  HS_ERR_UNSUPPORTED = 2,  /* valid request that this build cannot serve (device, size limit) */
+  HS_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed; see hs_last_error() */
+  HS_ERR_DEVICE_FLAG = 4,  /* returned by hs_check_flag when the device error flag is non-zero */
+  HS_ERR_TIMEOUT = 5       /* returned by hs_check_flag when HS_FLAG_TIMEOUT is set */
+} hs_status;
+
+/* Bits a kernel may OR into *err_flag. */
+#define HS_FLAG_BAD_INDEX      0x01  /* an index or physical row outside its valid range */
+#define HS_FLAG_BAD_LENGTH     0x02  /* a token_kvlen / seq_len outside [0, limit] */
+#define HS_FLAG_BAD_BLOCK      0x04  /* a block-table entry outside [0, nblk) */
+#define HS_FLAG_NOT_ASCENDING  0x08  /* resolve: a request's indices are not strictly ascending */
+#define HS_FLAG_BAD_STATE      0x10  /* resolve: inconsistent LRU state (slot/token maps disagree) */
+#define HS_FLAG_TIMEOUT        0x20  /* a bounded in-kernel wait ran out */
+
+#define HS_PAGE 64               /* tokens per KV page */
+#define HS_KV_ROW_BYTES 656      /* latent-KV row size */
+#define HS_D_LATENT 512          /* latent (value) width */
+#define HS_D_ROPE 64             /* RoPE width */
+#define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
+#define HS_ABI_VERSION 1
+
+int hs_abi_version(void);
+const char* hs_status_str(hs_status s);
+/* Text of the last error on the calling host thread ("" if none). Valid until the next call. */
+const char* hs_last_error(void);
+
+/* Copies *err_flag to the host (synchronising `stream`) and maps it to a status:
+ * 0 -> HS_OK, HS_FLAG_TIMEOUT set -> HS_ERR_TIMEOUT, other bits -> HS_ERR_DEVICE_FLAG.
+ * *flag_out (may be NULL) receives the raw bits. Convenience for tests; never used inside
+ * the other calls. */
+hs_status hs_check_flag(const int32_t* err_flag, int32_t* flag_out, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_indexer_scores — lightning-indexer scores.
+ *
+ * [P1] section 「DP8とTP8が不十分な理由」 and [P2] "¿Por qué no TP o DP?": the indexer scores
+ * every prior token to choose the 2,048 that sparse MLA attends; its cost is quadratic in the
+ * prompt length ([P1] 「PCP: ヘッドではなくトークンを分割」). Keys are 128-d FP8 with a 4-byte
+ * scale ([P1] 「数字がうまくいく理由」). The pages do not print the score formula; this library
+ * uses the DSA lightning-indexer form (ReLU of the FP8 dot product, weighted sum over index heads):
+ *
+ *   s[t, j] = sum_h  w[t,h] * max(0, q_scale[t,h] * k_scale[row(j)] * <q[t,h,:], k[row(j),:]>)
+ *
+ * for 0 <= j < token_kvlen[t] ("prior" includes the token itself), row(j) as in the paged layout
+ * of request token_req[t]. Columns j >= token_kvlen[t] are masked (-inf by definition) and are
+ * NOT written: callers read only j < token_kvlen[t].
+ *
+ * Requirements: q_scale > 0 and k_scale > 0 (the kernel folds them out of the ReLU).
+ * Tokens are processed in groups of 256/Hi consecutive tokens; a group may mix requests.
+ *
+ * Arguments (device pointers unless noted):
+ *   T, B          query tokens, requests (B >= 1)
+ *   Hi, Di        index heads in {8, 16, 32, 64}; head dim in {64, 128}
+ *   q             e4m3 [T, Hi, Di]
+ *   q_scale       fp32 [T, Hi]
+ *   weights       fp32 [T, Hi]
+ *   k_cache       e4m3 [nblk, 64, Di] (16-byte aligned)
+ *   k_scale       fp32 [nblk, 64]
+ *   block_table   int32 [B, bt_stride]
+ *   token_req     int32 [T], in [0, B)
+ *   token_kvlen   int32 [T], in [0, min(ld, bt_stride * 64)]
+ *   scores        fp32 [T, ld] (output)
+ *   err_flag      int32 (device)
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, B, Hi, Di;
+  const uint8_t* q;
+  const float* q_scale;
+  const float* weights;
+  const uint8_t* k_cache;
+  const float* k_scale;
+  int64_t nblk;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* token_req;
+  const int32_t* token_kvlen;
+  float* scores;
+  int64_t ld;
+  int32_t* err_flag;
+} hs_indexer_args;
+
+hs_status hs_indexer_scores(const hs_indexer_args* a, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_topk — per-query top-k selection.
+ *
+ * [P1] 「PCP: ヘッドではなくトークンを分割」: each query attends a fixed 2,048 tokens, chosen from
+ * the indexer scores. For query t with n = token_kvlen[t] visible scores, writes the
+ * min(k, n) indices j < n with the largest scores[t, j], in ascending index order, followed by
+ * -1 up to k. Order: larger score first; equal scores -> the lower index wins; -0.0 equals +0.0;
+ * NaN ranks below every number (-inf included).
+ *
+ *   scores       fp32 [T, ld] (device)       token_kvlen int32 [T], in [0, ld]
+ *   T, k         1 <= k <= 65536             idx int32 [T, k] (output)
+ * ---------------------------------------------------------------------------------------- */
+hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, int32_t T, int32_t k,
+                  int32_t* idx, int32_t* err_flag, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_sparse_mla_fwd — sparse MLA forward, MQA form (every KV row serves all heads).
+ *
+ * [P1] 「再現方法と必要なフラグ」 (sparse_mla_force_mqa) and 「数字がうまくいく理由」: each query
+ * reads its selected 656-byte FP8 latent rows once for all heads; QK runs over 576 dims, PV over
+ * 512. For query token t and head h, over the valid entries i of idx[t, :]:
+ *
+ *   logit_i = softmax_scale * ( sum_{c<512} q[t,h,c] * latent_i[c]  +  sum_{c<64} q[t,h,512+c] * rope_i[c] )
+ *   out[t,h,:] = sum_i softmax(logit)_i * latent_i[:]          (bf16, fp32 accumulation)
+ *   lse[t,h]   = ln sum_i exp(logit_i)                          (natural log; -inf if no row)
+ *
+ * idx entries < 0 are padding and skipped. With block_table == NULL they are physical pool rows
+ * (< R); otherwise logical token indices of request token_req[t] mapped through the paged layout.
+ * A query with no valid entry gets out = 0 and lse = -inf. Duplicated entries count once each.
+ *
+ *   T, H          query tokens; heads, 1 <= H <= 64
+ *   k             entries per idx row
+ *   q             bf16 [T, H, 576] (16-byte aligned)
+ *   kv_pool       uint8 [R, 656] (16-byte aligned)
+ *   idx           int32 [T, k]
+ *   block_table   int32 [B, bt_stride] or NULL; token_req int32 [T] (required with block_table)
+ *   out           bf16 [T, H, 512]
+ *   lse           fp32 [T, H] or NULL
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, H, k;
+  const uint16_t* q;
+  const uint8_t* kv_pool;
+  int64_t R;
+  const int32_t* idx;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* token_req;
+  float softmax_scale;
+  uint16_t* out;
+  float* lse;
+  int32_t* err_flag;
+} hs_mla_args;
+
+hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_hisparse_resolve — Hybrid HiSparse top-k resolve ("mixed residency").
+ *
+ * [P3] section 「ハイブリッド HiSparse の技術的実装」, item 2: one kernel resolves the top-k of a
+ * request whose tail is GPU-resident and whose older pages live in host memory: resident tokens
+ * are read as they are, hot tokens are read while their LRU entry is refreshed, and a miss copies
+ * one row from pinned host memory into an LRU slot. [P3] 「主要なアーキテクチャ的詳細」: hot
+ * buffers are ordinary KV blocks borrowed from the shared pool, 2 x top-k rows per request by
+ * default. For each request r (one step):
+ *   1. Classify each valid idx[r, i] (i in list order): j >= resident_start[r] -> resident, row =
+ *      paged row of j; else tok2slot[r, j] >= 0 -> hit, row = slot_row[r, slot]; else miss.
+ *   2. Every hit slot gets slot_stamp = step.
+ *   3. The m misses take the m slots not hit this step with the smallest (slot_stamp, slot)
+ *      pairs (an empty slot has stamp -1 and token -1, so empty slots go first).
+ *   4. The i-th miss in ascending token order takes the i-th such slot: the evicted token's
+ *      tok2slot entry becomes -1, the slot gets the new token, tok2slot maps it, its stamp
+ *      becomes step, and the 656-byte row j of host_rows[r] is copied to pool row slot_row[slot].
+ *   5. out_rows[r, i] = the physical row of entry i (-1 for padding); counters[r] =
+ *      {resident, hit, miss}.
+ *
+ * Requirements: valid entries of each idx row are strictly ascending, followed only by -1;
+ * k <= S <= 8192; step is larger than every stamp already in the state; slot_row entries are
+ * distinct pool rows that no resident page uses.
+ *
+ *   B, k, S, step  requests, idx columns, hot slots per request, step number (>= 0)
+ *   idx            int32 [B, k]           seq_len int32 [B]     resident_start int32 [B]
+ *   block_table    int32 [B, bt_stride]   (pages of resident tokens, indexed by absolute page)
+ *   host_rows      device array of B device-accessible pointers, each to pinned uint8 [seq_len, 656]
+ *   kv_pool        uint8 [R, 656]
+ *   slot_row       int32 [B, S]   slot_token int32 [B, S]   slot_stamp int32 [B, S]  (in/out)
+ *   tok2slot       int32 [B, ld_t2s], ld_t2s >= max seq_len (in/out)
+ *   out_rows       int32 [B, k]   counters int32 [B, 3] (outputs)
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t B, k, S, step;
+  const int32_t* idx;
+  const int32_t* seq_len;
+  const int32_t* resident_start;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const uint8_t* const* host_rows;
+  uint8_t* kv_pool;
+  int64_t R;
+  const int32_t* slot_row;
+  int32_t* slot_token;
+  int32_t* slot_stamp;
+  int32_t* tok2slot;
+  int64_t ld_t2s;
+  int32_t* out_rows;
+  int32_t* counters;
+  int32_t* err_flag;
+} hs_resolve_args;
+
+hs_status hs_hisparse_resolve(const hs_resolve_args* a, hs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HS_H_ */
