@@ -1,0 +1,182 @@
+"""GB300-native sparse MLA (DeepSeek sparse attention) hot path.
+
+Thin Python binding of ``libhs.so`` (C ABI in ``include/hs.h``): the functions below have the
+C names, take torch CUDA tensors, marshal pointers and sizes, and call the library on the
+current (or given) CUDA stream. Every step of the computation runs in the library's sm_103a
+kernels; there is no fallback. If the library is missing, import succeeds but every call raises
+``HSError`` telling how to build it (``python -m dsa_sparse_mla_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
+           "hs_sparse_mla_fwd", "hs_hisparse_resolve", "FLAGS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libhs.so")
+_lib = None
+
+FLAGS = {"BAD_INDEX": 0x01, "BAD_LENGTH": 0x02, "BAD_BLOCK": 0x04, "NOT_ASCENDING": 0x08, "BAD_STATE": 0x10,
+         "TIMEOUT": 0x20}
+_STATUS = {0: "HS_OK", 1: "HS_ERR_INVALID", 2: "HS_ERR_UNSUPPORTED", 3: "HS_ERR_CUDA", 4: "HS_ERR_DEVICE_FLAG",
+           5: "HS_ERR_TIMEOUT"}
+
+
+class HSError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (_STATUS.get(status, status), message))
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_i32, _i64, _f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+
+
+class _IndexerArgs(ctypes.Structure):
+    _fields_ = [("T", _i32), ("B", _i32), ("Hi", _i32), ("Di", _i32), ("q", _P), ("q_scale", _P), ("weights", _P),
+                ("k_cache", _P), ("k_scale", _P), ("nblk", _i64), ("block_table", _P), ("bt_stride", _i32),
+                ("token_req", _P), ("token_kvlen", _P), ("scores", _P), ("ld", _i64), ("err_flag", _P)]
+
+
+class _MlaArgs(ctypes.Structure):
+    _fields_ = [("T", _i32), ("H", _i32), ("k", _i32), ("q", _P), ("kv_pool", _P), ("R", _i64), ("idx", _P),
+                ("block_table", _P), ("bt_stride", _i32), ("token_req", _P), ("softmax_scale", _f32),
+                ("out", _P), ("lse", _P), ("err_flag", _P)]
+
+
+class _ResolveArgs(ctypes.Structure):
+    _fields_ = [("B", _i32), ("k", _i32), ("S", _i32), ("step", _i32), ("idx", _P), ("seq_len", _P),
+                ("resident_start", _P), ("block_table", _P), ("bt_stride", _i32), ("host_rows", _P),
+                ("kv_pool", _P), ("R", _i64), ("slot_row", _P), ("slot_token", _P), ("slot_stamp", _P),
+                ("tok2slot", _P), ("ld_t2s", _i64), ("out_rows", _P), ("counters", _P), ("err_flag", _P)]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libhs.so once. Raises HSError if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise HSError(2, "libhs.so not found at %s; build it with `python -m dsa_sparse_mla_gb300.build`"
+                          % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.hs_abi_version.restype = ctypes.c_int
+        lib.hs_status_str.argtypes = [ctypes.c_int]
+        lib.hs_status_str.restype = ctypes.c_char_p
+        lib.hs_last_error.restype = ctypes.c_char_p
+        lib.hs_check_flag.argtypes = [_P, _P, _P]
+        lib.hs_indexer_scores.argtypes = [ctypes.POINTER(_IndexerArgs), _P]
+        lib.hs_topk.argtypes = [_P, _i64, _P, _i32, _i32, _P, _P, _P]
+        lib.hs_sparse_mla_fwd.argtypes = [ctypes.POINTER(_MlaArgs), _P]
+        lib.hs_hisparse_resolve.argtypes = [ctypes.POINTER(_ResolveArgs), _P]
+        for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_hisparse_resolve"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise HSError(status, load().hs_last_error().decode(errors="replace"))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise HSError(1, "%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise HSError(1, "%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise HSError(1, "%s must be %s (got %s)" % (name, dtype, t.dtype))
+    return t
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def hs_abi_version() -> int:
+    return int(load().hs_abi_version())
+
+
+def hs_check_flag(err_flag: torch.Tensor, stream=None) -> int:
+    """Synchronise `stream` and return the raw device error bits (0 = none)."""
+    out = ctypes.c_int32(0)
+    st = load().hs_check_flag(_ptr(_dev(err_flag, "err_flag", torch.int32)), ctypes.addressof(out), _stream(stream))
+    if st not in (0, 4, 5):
+        _check(st)
+    return int(out.value)
+
+
+def hs_indexer_scores(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, err_flag,
+                      num_requests: int | None = None, stream=None):
+    """Lightning-indexer scores into ``scores`` (float32 [T, ld]); see include/hs.h."""
+    _dev(q, "q", torch.uint8), _dev(q_scale, "q_scale", torch.float32), _dev(weights, "weights", torch.float32)
+    _dev(k_cache, "k_cache", torch.uint8), _dev(k_scale, "k_scale", torch.float32)
+    _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
+    _dev(token_kvlen, "token_kvlen", torch.int32), _dev(scores, "scores", torch.float32)
+    _dev(err_flag, "err_flag", torch.int32)
+    T, Hi, Di = q.shape
+    a = _IndexerArgs(T, num_requests if num_requests is not None else block_table.shape[0], Hi, Di, _ptr(q),
+                     _ptr(q_scale), _ptr(weights), _ptr(k_cache), _ptr(k_scale), k_cache.shape[0],
+                     _ptr(block_table), block_table.shape[1], _ptr(token_req), _ptr(token_kvlen), _ptr(scores),
+                     scores.shape[1], _ptr(err_flag))
+    _check(load().hs_indexer_scores(ctypes.byref(a), _stream(stream)))
+
+
+def hs_topk(scores, token_kvlen, k: int, idx, err_flag, stream=None):
+    """Top-k indices (ascending, -1 padded) into ``idx`` (int32 [T, k])."""
+    _dev(scores, "scores", torch.float32), _dev(token_kvlen, "token_kvlen", torch.int32)
+    _dev(idx, "idx", torch.int32), _dev(err_flag, "err_flag", torch.int32)
+    T, ld = scores.shape
+    if idx.shape != (T, k):
+        raise HSError(1, "idx must have shape [T, k]")
+    _check(load().hs_topk(_ptr(scores), ld, _ptr(token_kvlen), T, k, _ptr(idx), _ptr(err_flag), _stream(stream)))
+
+
+def hs_sparse_mla_fwd(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=None, block_table=None,
+                      token_req=None, stream=None):
+    """Sparse MLA forward: ``out`` bf16 [T, H, 512] (and ``lse`` float32 [T, H] if given)."""
+    _dev(q, "q", torch.bfloat16), _dev(kv_pool, "kv_pool", torch.uint8), _dev(idx, "idx", torch.int32)
+    _dev(out, "out", torch.bfloat16), _dev(err_flag, "err_flag", torch.int32), _dev(lse, "lse", torch.float32)
+    _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
+    T, H, D = q.shape
+    if D != 576 or kv_pool.shape[-1] != 656 or out.shape != (T, H, 512) or idx.shape[0] != T:
+        raise HSError(1, "shape mismatch: q [T,H,576], kv_pool [R,656], idx [T,k], out [T,H,512]")
+    a = _MlaArgs(T, H, idx.shape[1], _ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(idx), _ptr(block_table),
+                 0 if block_table is None else block_table.shape[1], _ptr(token_req), float(softmax_scale),
+                 _ptr(out), _ptr(lse), _ptr(err_flag))
+    _check(load().hs_sparse_mla_fwd(ctypes.byref(a), _stream(stream)))
+
+
+def hs_hisparse_resolve(step: int, idx, seq_len, resident_start, block_table, host_rows, kv_pool, slot_row,
+                        slot_token, slot_stamp, tok2slot, out_rows, counters, err_flag, stream=None):
+    """One HiSparse resolve step. ``host_rows`` is an int64 CUDA tensor [B] of device-accessible
+    pointers to each request's pinned host rows [seq_len, 656]."""
+    for t, n, dt in ((idx, "idx", torch.int32), (seq_len, "seq_len", torch.int32),
+                     (resident_start, "resident_start", torch.int32), (block_table, "block_table", torch.int32),
+                     (host_rows, "host_rows", torch.int64), (kv_pool, "kv_pool", torch.uint8),
+                     (slot_row, "slot_row", torch.int32), (slot_token, "slot_token", torch.int32),
+                     (slot_stamp, "slot_stamp", torch.int32), (tok2slot, "tok2slot", torch.int32),
+                     (out_rows, "out_rows", torch.int32), (counters, "counters", torch.int32),
+                     (err_flag, "err_flag", torch.int32)):
+        _dev(t, n, dt)
+    B, k = idx.shape
+    a = _ResolveArgs(B, k, slot_row.shape[1], int(step), _ptr(idx), _ptr(seq_len), _ptr(resident_start),
+                     _ptr(block_table), block_table.shape[1], _ptr(host_rows), _ptr(kv_pool), kv_pool.shape[0],
+                     _ptr(slot_row), _ptr(slot_token), _ptr(slot_stamp), _ptr(tok2slot), tok2slot.shape[1],
+                     _ptr(out_rows), _ptr(counters), _ptr(err_flag))
+    _check(load().hs_hisparse_resolve(ctypes.byref(a), _stream(stream)))

@@ -1,0 +1,385 @@
+// indexer.cu — lightning-indexer scores as an FP8 tcgen05 GEMM with a fused epilogue.
+//
+// [P1] "vLLM v0.32.0 GLM-5.3 サービング ...", section 「DP8とTP8が不十分な理由」: the indexer
+// scores every prior token to pick the tokens sparse MLA attends; section 「数字がうまくいく理由」:
+// keys are 128 FP8 values with a 4-byte scale. Score (DSA lightning-indexer form):
+//   s[t, j] = sum_h w[t,h] * max(0, q_scale[t,h] * k_scale[j] * <q[t,h,:], k[j,:]>),  j < n_t.
+// Since both scales are positive, s = k_scale[j] * sum_h (w*q_scale)[t,h] * max(0, <q, k>):
+// the GEMM runs on raw e4m3 codes and the scales are applied in the epilogue.
+//
+// Work split: a CTA owns one group of 256/Hi consecutive query tokens (so the MMA's N is
+// tokens x heads = 256) and a contiguous range of 128-key tiles of each request in the group.
+// Keys sit on the MMA's M (TMEM lanes), so each epilogue thread owns one key and does the ReLU,
+// the weighted head sum and the causal mask in registers, then writes one coalesced score.
+//
+// Roles (320 threads): warp 0 issues TMA loads (query tile once, two 64-key pages per stage),
+// warp 1 allocates TMEM and issues tcgen05.mma (e4m3 x e4m3 -> fp32, M=128, N=256, K=32),
+// warps 2..9 drain the two TMEM accumulators (each warp: its 32-lane quarter, half the columns).
+#include "common.cuh"
+
+namespace hs {
+namespace indexer {
+
+constexpr int kBlockM = 128;   // keys per tile (two pages)
+constexpr int kN = 256;        // (token, head) columns per group
+constexpr int kStages = 6;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kMaxG = 32;      // tokens per group when Hi = 8
+
+struct Params {
+  int32_t T, B, Hi, Di;
+  const float* q_scale;
+  const float* weights;
+  const float* k_scale;
+  int64_t nblk;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* token_req;
+  const int32_t* token_kvlen;
+  float* scores;
+  int64_t ld;
+  int32_t* err;
+  int32_t tiles_per_cta;
+};
+
+template <int DI, int HI>
+struct Cfg {
+  static constexpr int G = kN / HI;
+  static constexpr int kTileBytes = kBlockM * DI;
+  static constexpr int kQBytes = kN * DI;
+  static constexpr uint32_t kSwizzle = DI == 128 ? 2u : 4u;  // 128-byte / 64-byte swizzle
+  static constexpr uint32_t kSBO = 8 * DI;                    // one 8-row swizzle atom
+  static constexpr int kKSteps = DI / 32;                     // K = 32 per e4m3 MMA
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffW = kOffK + kStages * kTileBytes;
+  static constexpr int kOffTok = kOffW + kN * 4;              // int32 x 4 x kMaxG
+  static constexpr int kOffSeg = kOffTok + 4 * kMaxG * 4;     // int32 x 4 x kMaxG
+  static constexpr int kOffBar = kOffSeg + 4 * kMaxG * 4;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmem = kOffMisc + 64 + 1024;          // + alignment slack
+};
+
+template <int DI, int HI>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                   const Params p) {
+  using C = Cfg<DI, HI>;
+  constexpr int G = C::G;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sK = smem + C::kOffK;
+  float* sW = (float*)(smem + C::kOffW);                 // (w * q_scale) [G][HI]
+  int32_t* sTokN = (int32_t*)(smem + C::kOffTok);        // visible keys per token (0 = skip)
+  int32_t* sTokSeg = sTokN + kMaxG;                      // segment of each token (-1 = none)
+  int32_t* sSegReq = (int32_t*)(smem + C::kOffSeg);      // request of each segment
+  int32_t* sSegN = sSegReq + kMaxG;                      // max visible keys in the segment
+  int32_t* sSegLo = sSegN + kMaxG;                       // first tile of this CTA
+  int32_t* sSegHi = sSegLo + kMaxG;                      // one past the last tile
+  uint64_t* bars = (uint64_t*)(smem + C::kOffBar);
+  uint64_t* full = bars;                                 // [kStages]
+  uint64_t* empty = bars + kStages;                      // [kStages]
+  uint64_t* acc_full = bars + 2 * kStages;               // [2]
+  uint64_t* acc_empty = acc_full + 2;                    // [2]
+  uint64_t* q_full = acc_empty + 2;
+  uint64_t* mma_done = q_full + 1;
+  int32_t* misc = (int32_t*)(smem + C::kOffMisc);        // [0] nseg, [1] abort, [2] tmem base
+  volatile int32_t* abort_flag = misc + 1;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int group = blockIdx.x, split = blockIdx.y;
+  const int t0 = group * G;
+
+  // ---------------- setup: token metadata, folded weights, segments, barriers, TMEM -------------
+  if (tid < G) {
+    const int t = t0 + tid;
+    int32_t n = 0, r = -1;
+    if (t < p.T) {
+      r = p.token_req[t];
+      n = p.token_kvlen[t];
+      const int64_t nmax = p.ld < (int64_t)p.bt_stride * 64 ? p.ld : (int64_t)p.bt_stride * 64;
+      if (r < 0 || r >= p.B) {
+        flag_error(p.err, HS_FLAG_BAD_INDEX);
+        n = 0;
+      } else if (n < 0 || (int64_t)n > nmax) {
+        flag_error(p.err, HS_FLAG_BAD_LENGTH);
+        n = 0;
+      }
+    }
+    sTokN[tid] = n;
+    sTokSeg[tid] = (n > 0) ? r : -1;  // request for now; turned into a segment id below
+  }
+  if (tid < G * HI) {
+    const int g = tid / HI, h = tid % HI, t = t0 + g;
+    sW[tid] = (t < p.T) ? p.weights[(int64_t)t * HI + h] * p.q_scale[(int64_t)t * HI + h] : 0.f;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(mma_done, 1);
+    mbar_fence_init();
+    misc[1] = 0;
+  }
+  if (warp == 1) tmem_alloc((uint32_t*)&misc[2], 512);
+  __syncthreads();
+  if (tid == 0) {
+    int nseg = 0;
+    for (int g = 0; g < G; ++g) {
+      const int r = sTokSeg[g];
+      if (r < 0) continue;
+      int s = 0;
+      while (s < nseg && sSegReq[s] != r) ++s;
+      if (s == nseg) {
+        sSegReq[s] = r;
+        sSegN[s] = 0;
+        ++nseg;
+      }
+      sTokSeg[g] = s;
+      if (sTokN[g] > sSegN[s]) sSegN[s] = sTokN[g];
+    }
+    for (int s = 0; s < nseg; ++s) {
+      const int tiles = (sSegN[s] + kBlockM - 1) / kBlockM;
+      const int lo = split * p.tiles_per_cta;
+      int hi = lo + p.tiles_per_cta;
+      if (hi > tiles) hi = tiles;
+      sSegLo[s] = lo;
+      sSegHi[s] = hi > lo ? hi : lo;
+    }
+    misc[0] = nseg;
+  }
+  __syncthreads();
+  tc_fence_after();
+  const int nseg = misc[0];
+  const uint32_t tmem = (uint32_t)misc[2];
+  int total = 0;
+  for (int s = 0; s < nseg; ++s) total += sSegHi[s] - sSegLo[s];
+
+  if (total > 0) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer ----------------
+      if (lane == 0) {
+        prefetch_tensormap(&map_q);
+        prefetch_tensormap(&map_k);
+        mbar_arrive_expect_tx(q_full, C::kQBytes);
+        tma_load_2d(sQ, &map_q, q_full, 0, t0 * HI);
+        int it = 0;
+        for (int s = 0; s < nseg && !*abort_flag; ++s) {
+          const int r = sSegReq[s];
+          for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
+            const int st = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            if (!mbar_wait(&empty[st], ph ^ 1u, p.err)) {
+              *abort_flag = 1;
+              break;
+            }
+            int32_t blk[2];
+            uint32_t bytes = 0;
+            for (int pg = 0; pg < 2; ++pg) {
+              const int page = 2 * kt + pg;
+              blk[pg] = -1;
+              if (page * 64 < sSegN[s]) {
+                const int32_t b = p.block_table[(int64_t)r * p.bt_stride + page];
+                if (b >= 0 && (int64_t)b < p.nblk) {
+                  blk[pg] = b;
+                  bytes += 64 * DI;
+                } else {
+                  flag_error(p.err, HS_FLAG_BAD_BLOCK);
+                }
+              }
+            }
+            mbar_arrive_expect_tx(&full[st], bytes);
+            for (int pg = 0; pg < 2; ++pg)
+              if (blk[pg] >= 0)
+                tma_load_2d(sK + st * C::kTileBytes + pg * 64 * DI, &map_k, &full[st], 0, blk[pg] * 64);
+          }
+        }
+        // every issued copy must land before the CTA's shared memory is released
+        mbar_wait(q_full, 0, p.err);
+        for (int i = it > kStages ? it - kStages : 0; i < it; ++i)
+          mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, p.err);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer ------------------
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3(kBlockM, kN);
+        const uint32_t q_addr = smem_u32(sQ);
+        const uint32_t k_addr = smem_u32(sK);
+        bool ok = mbar_wait(q_full, 0, p.err);
+        int it = 0;
+        for (int s = 0; s < nseg && ok && !*abort_flag; ++s) {
+          for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
+            const int st = it % kStages;
+            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+            const int b = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(&full[st], ph, p.err) || !mbar_wait(&acc_empty[b], aph ^ 1u, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < C::kKSteps; ++ks) {
+              const uint64_t a = smem_desc(k_addr + st * C::kTileBytes + ks * 32, 16, C::kSBO, C::kSwizzle);
+              const uint64_t bq = smem_desc(q_addr + ks * 32, 16, C::kSBO, C::kSwizzle);
+              mma_e4m3_ss(tmem + (uint32_t)(b * kN), a, bq, idesc, ks > 0 ? 1u : 0u);
+            }
+            mma_commit(&empty[st]);
+            mma_commit(&acc_full[b]);
+          }
+        }
+        if (!ok) *abort_flag = 1;
+        // all issued MMAs must finish before TMEM is released
+        mma_commit(mma_done);
+        mbar_wait(mma_done, 0, p.err);
+      }
+    } else {
+      // ------------------------------------------------------------ epilogue --------------------
+      const int quad = warp & 3;
+      const int half = (warp - 2) >> 2;
+      const int row = quad * 32 + lane;
+      int it = 0;
+      bool run = true;
+      for (int s = 0; s < nseg && run; ++s) {
+        const int r = sSegReq[s];
+        const int segn = sSegN[s];
+        for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
+          const int b = it & 1;
+          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+          const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
+          if (!__all_sync(0xffffffffu, go)) {
+            *abort_flag = 1;
+            run = false;
+            break;
+          }
+          tc_fence_after();
+          const int64_t j = (int64_t)kt * kBlockM + row;
+          float ks = 0.f;
+          bool key_ok = false;
+          if (j < segn) {
+            const int32_t blk = p.block_table[(int64_t)r * p.bt_stride + (j >> 6)];
+            if (blk >= 0 && (int64_t)blk < p.nblk) {
+              ks = p.k_scale[(int64_t)blk * 64 + (j & 63)];
+              key_ok = true;
+            }
+          }
+#pragma unroll 1
+          for (int gi = 0; gi < G / 2; ++gi) {
+            const int g = half * (G / 2) + gi;
+            if (sTokSeg[g] != s) continue;  // warp-uniform
+            uint32_t acc[HI];
+            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kN + g * HI);
+            if constexpr (HI >= 32) {
+#pragma unroll
+              for (int c = 0; c < HI; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
+            } else {
+#pragma unroll
+              for (int c = 0; c < HI; c += 8) tmem_ld8(taddr + c, *reinterpret_cast<uint32_t(*)[8]>(&acc[c]));
+            }
+            tmem_wait_ld();
+            const float* w = sW + g * HI;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < HI; h += 2) {
+              const float2 wv = *reinterpret_cast<const float2*>(w + h);
+              s0 = fmaf(wv.x, fmaxf(__uint_as_float(acc[h]), 0.f), s0);
+              s1 = fmaf(wv.y, fmaxf(__uint_as_float(acc[h + 1]), 0.f), s1);
+            }
+            if (key_ok && j < sTokN[g]) p.scores[(int64_t)(t0 + g) * p.ld + j] = ks * (s0 + s1);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
+      }
+    }
+  }
+  // ---------------- teardown: wait for outstanding MMAs, release TMEM -------------------------------
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DI, int HI>
+static cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const Params& p, int groups, int splits,
+                            cudaStream_t stream) {
+  using C = Cfg<DI, HI>;
+  auto kern = indexer_kernel<DI, HI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(groups, splits), kThreads, C::kSmem, stream>>>(mq, mk, p);
+  return cudaGetLastError();
+}
+
+}  // namespace indexer
+
+// Called by the C ABI after argument checks. Encodes the tensor maps and launches.
+cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t stream, const char** why) {
+  using namespace indexer;
+  CUtensorMap mq, mk;
+  const int DI = a->Di, HI = a->Hi;
+  const CUtensorMapSwizzle sw = DI == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (!encode_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->q, DI, (uint64_t)a->T * HI, DI, DI, kN, sw)) {
+    *why = "cuTensorMapEncodeTiled failed for q";
+    return cudaErrorInvalidValue;
+  }
+  if (!encode_2d(&mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->k_cache, DI, (uint64_t)a->nblk * 64, DI, DI, 64, sw)) {
+    *why = "cuTensorMapEncodeTiled failed for k_cache";
+    return cudaErrorInvalidValue;
+  }
+  Params p;
+  p.T = a->T;
+  p.B = a->B;
+  p.Hi = HI;
+  p.Di = DI;
+  p.q_scale = a->q_scale;
+  p.weights = a->weights;
+  p.k_scale = a->k_scale;
+  p.nblk = a->nblk;
+  p.block_table = a->block_table;
+  p.bt_stride = a->bt_stride;
+  p.token_req = a->token_req;
+  p.token_kvlen = a->token_kvlen;
+  p.scores = a->scores;
+  p.ld = a->ld;
+  p.err = a->err_flag;
+  const int G = kN / HI;
+  const int groups = (a->T + G - 1) / G;
+  const int64_t keys_max = a->ld < (int64_t)a->bt_stride * 64 ? a->ld : (int64_t)a->bt_stride * 64;
+  const int tiles_max = (int)((keys_max + kBlockM - 1) / kBlockM);
+  // about three CTAs' worth of tiles per SM over the whole grid, 8..64 tiles each
+  int64_t tpc = ((int64_t)groups * tiles_max + 3LL * num_sms - 1) / (3LL * num_sms);
+  if (tpc < 8) tpc = 8;
+  if (tpc > 64) tpc = 64;
+  p.tiles_per_cta = (int)tpc;
+  int splits = (int)((tiles_max + tpc - 1) / tpc);
+  if (splits < 1) splits = 1;
+  if (groups == 0) return cudaSuccess;
+#define HS_IDX_CASE(D, H) \
+  if (DI == D && HI == H) return launch_t<D, H>(mq, mk, p, groups, splits, stream);
+  HS_IDX_CASE(128, 64)
+  HS_IDX_CASE(128, 32)
+  HS_IDX_CASE(128, 16)
+  HS_IDX_CASE(128, 8)
+  HS_IDX_CASE(64, 64)
+  HS_IDX_CASE(64, 32)
+  HS_IDX_CASE(64, 16)
+  HS_IDX_CASE(64, 8)
+#undef HS_IDX_CASE
+  *why = "unsupported (Hi, Di)";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hs

@@ -128,7 +128,10 @@ def pack_kv_rows(latent: np.ndarray, rope: np.ndarray, group_scales: np.ndarray 
         gs = np.repeat(scale[:, None], 4, axis=1).astype(np.float32)
     else:
         gs = np.ascontiguousarray(group_scales, dtype=np.float32)
-        codes = e4m3_encode(latent / np.repeat(gs, 128, axis=1))
+        scaled = latent / np.repeat(gs, 128, axis=1)
+        if np.abs(scaled).max() > E4M3_MAX:
+            raise ValueError("group scales too small: |latent / scale| exceeds the e4m3 range (448)")
+        codes = e4m3_encode(scaled)
     rows[:, :D_LATENT] = codes
     rows[:, D_LATENT:D_LATENT + 16] = gs.view(np.uint8).reshape(n, 16)
     rows[:, D_LATENT + 16:] = bf16_bits(rope).view(np.uint8).reshape(n, 2 * D_ROPE)

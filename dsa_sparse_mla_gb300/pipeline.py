@@ -1,0 +1,130 @@
+"""Device-side driver of the hot path.
+
+``DeviceWorkload`` moves a seeded ``inputs.Workload`` into GPU memory; ``HotPath`` owns the
+intermediate and output buffers and runs one step: hs_indexer_scores -> hs_topk ->
+hs_sparse_mla_fwd (logical indices through the paged block table). ``DeviceHiSparse`` does the
+same for the mixed-residency decode (hs_hisparse_resolve -> hs_sparse_mla_fwd on physical rows),
+with the older rows in pinned host memory.
+
+Only buffer management lives here; all arithmetic runs in libhs.so.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from . import (hs_hisparse_resolve, hs_indexer_scores, hs_sparse_mla_fwd, hs_topk)
+from .inputs import HiSparseWorkload, Workload
+
+
+def _t(a: np.ndarray, device, dtype=None) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(device)
+
+
+@dataclasses.dataclass
+class DeviceWorkload:
+    w: Workload
+    q_idx: torch.Tensor
+    q_scale: torch.Tensor
+    weights: torch.Tensor
+    k_cache: torch.Tensor
+    k_scale: torch.Tensor
+    block_table: torch.Tensor
+    token_req: torch.Tensor
+    token_kvlen: torch.Tensor
+    q_mla: torch.Tensor
+    kv_pool: torch.Tensor
+
+    @classmethod
+    def from_host(cls, w: Workload, device="cuda") -> "DeviceWorkload":
+        return cls(w, _t(w.q_idx, device), _t(w.q_scale, device), _t(w.weights, device), _t(w.k_cache, device),
+                   _t(w.k_scale, device), _t(w.block_table, device), _t(w.token_req, device),
+                   _t(w.token_kvlen, device), _t(w.q_mla.view(np.int16), device).view(torch.bfloat16),
+                   _t(w.kv_pool, device))
+
+
+class HotPath:
+    """Buffers and launches for one step of indexer -> top-k -> sparse MLA."""
+
+    def __init__(self, dw: DeviceWorkload):
+        w = dw.w
+        dev = dw.q_idx.device
+        self.dw = dw
+        self.scores = torch.empty((w.T, w.ld), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((w.T, w.topk), dtype=torch.int32, device=dev)
+        self.out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def indexer(self, stream=None):
+        d = self.dw
+        hs_indexer_scores(d.q_idx, d.q_scale, d.weights, d.k_cache, d.k_scale, d.block_table, d.token_req,
+                          d.token_kvlen, self.scores, self.err, num_requests=d.w.B, stream=stream)
+
+    def topk(self, stream=None):
+        hs_topk(self.scores, self.dw.token_kvlen, self.dw.w.topk, self.idx, self.err, stream=stream)
+
+    def mla(self, stream=None):
+        d = self.dw
+        hs_sparse_mla_fwd(d.q_mla, d.kv_pool, self.idx, d.w.softmax_scale, self.out, self.err, lse=self.lse,
+                          block_table=d.block_table, token_req=d.token_req, stream=stream)
+
+    def step(self, stream=None):
+        self.indexer(stream)
+        self.topk(stream)
+        self.mla(stream)
+
+
+def pinned_uint8(nbytes: int) -> np.ndarray:
+    """Page-locked host buffer (device-accessible through unified addressing) as a numpy view.
+    The torch tensor owning the memory is kept alive by the returned array's base chain."""
+    t = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    a = t.numpy()
+    _PINNED_KEEPALIVE.append(t)
+    return a
+
+
+_PINNED_KEEPALIVE: list = []
+
+
+class DeviceHiSparse:
+    """Device state of the mixed-residency decode: pool, block table, LRU state, index stream."""
+
+    def __init__(self, hw: HiSparseWorkload, device="cuda"):
+        self.hw = hw
+        B, S, k = hw.B, hw.S, hw.k
+        self.kv_pool = _t(hw.kv_pool, device)
+        self.block_table = _t(hw.block_table, device)
+        self.seq_len = _t(hw.seq_len, device)
+        self.resident_start = _t(hw.resident_start, device)
+        self.slot_row = _t(hw.slot_row, device)
+        self.slot_token = torch.full((B, S), -1, dtype=torch.int32, device=device)
+        self.slot_stamp = torch.full((B, S), -1, dtype=torch.int32, device=device)
+        self.ld_t2s = int(hw.seq_len.max())
+        self.tok2slot = torch.full((B, self.ld_t2s), -1, dtype=torch.int32, device=device)
+        self.host_rows = torch.tensor([int(h.ctypes.data) for h in hw.host_rows], dtype=torch.int64, device=device)
+        self.idx = _t(hw.idx, device)                                     # [steps, B, k]
+        self.q = _t(hw.q_mla.view(np.int16), device).view(torch.bfloat16)  # [steps, B, H, 576]
+        self.rows = torch.empty((B, k), dtype=torch.int32, device=device)
+        self.counters = torch.zeros((B, 3), dtype=torch.int32, device=device)
+        self.out = torch.empty((B, hw.H, 512), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((B, hw.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def resolve(self, step: int, stream=None):
+        hs_hisparse_resolve(step, self.idx[step], self.seq_len, self.resident_start, self.block_table,
+                            self.host_rows, self.kv_pool, self.slot_row, self.slot_token, self.slot_stamp,
+                            self.tok2slot, self.rows, self.counters, self.err, stream=stream)
+
+    def mla(self, step: int, stream=None):
+        hs_sparse_mla_fwd(self.q[step], self.kv_pool, self.rows, self.hw.softmax_scale, self.out, self.err,
+                          lse=self.lse, stream=stream)
+
+    def step(self, step: int, stream=None):
+        self.resolve(step, stream)
+        self.mla(step, stream)

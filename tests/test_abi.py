@@ -1,0 +1,67 @@
+"""The C-ABI library builds and exports every function include/hs.h declares (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dsa_sparse_mla_gb300 as hs
+from dsa_sparse_mla_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "hs.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:hs_status|int|const char\*)\s+(hs_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_four_calls():
+    names = _declared()
+    for n in ("hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_hisparse_resolve"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert hs.hs_abi_version() == 1
+    hs.load()
+    for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
+                                 "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
+        assert hs.load().hs_status_str(code).decode() == name
+
+
+def test_invalid_arguments_rejected_before_any_device_work(lib):
+    """Host-side checks fail with HS_ERR_INVALID and a message, without touching a GPU."""
+    L = hs.load()
+    st = L.hs_topk(None, 10, None, 1, 0, None, None, None)          # k = 0
+    assert st == 1 and b"k must be" in L.hs_last_error()
+    a = hs._IndexerArgs()
+    a.T, a.B, a.Hi, a.Di = 4, 1, 12, 128                              # Hi = 12
+    assert L.hs_indexer_scores(ctypes.byref(a), None) == 1 and b"Hi" in L.hs_last_error()
+    m = hs._MlaArgs()
+    m.T, m.H, m.k = 1, 0, 1
+    assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1
+    r = hs._ResolveArgs()
+    r.B, r.k, r.S, r.step = 1, 9, 8, 0                                # k > S
+    assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1
+    r.k, r.S = 8, 9000                                                # S too large
+    assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1
+
+
+def test_calls_without_library_fail_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(hs, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(hs, "_lib", None)
+    with pytest.raises(hs.HSError):
+        hs.load()

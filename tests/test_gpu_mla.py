@@ -1,0 +1,103 @@
+"""GPU parity of hs_sparse_mla_fwd against the oracle run on the same index set."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_mla_gb300 import HSError, hs_check_flag, hs_sparse_mla_fwd, inputs
+
+from parity import check_mla
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(n, seed, group_scales=False):
+    st = inputs.Stream(seed)
+    lat = st.sub("l").normal((n, 512))
+    rope = st.sub("r").normal((n, 64))
+    gs = None
+    if group_scales:
+        gs = (np.abs(lat).reshape(n, 4, 128).max(-1) / 448 * np.array([1.0, 3.0, 1.5, 7.0])).astype(np.float32)
+    return inputs.pack_kv_rows(lat, rope, gs)
+
+
+def _run(q_bits, kv, idx, scale, bt=None, req=None):
+    T, H, _ = q_bits.shape
+    q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    kvt = torch.from_numpy(kv).cuda()
+    it = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda()
+    out = torch.full((T, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    btt = None if bt is None else torch.from_numpy(bt).cuda()
+    rt = None if req is None else torch.from_numpy(req).cuda()
+    hs_sparse_mla_fwd(q, kvt, it, scale, out, err, lse=lse, block_table=btt, token_req=rt)
+    flag = hs_check_flag(err)
+    return out, lse, flag
+
+
+@pytest.mark.parametrize("H,k,n", [(64, 2048, 5000), (64, 130, 300), (16, 256, 1024), (64, 64, 64), (1, 1, 1),
+                                   (40, 200, 777)])
+def test_random_index_sets(H, k, n):
+    rng = np.random.default_rng(H * 1000 + k)
+    T = 7
+    kv = _rows(n, seed=k + n)
+    q = inputs.bf16_bits(inputs.Stream(n).sub("q").normal((T, H, 576)))
+    idx = np.stack([rng.permutation(n)[:k] if k <= n else rng.integers(0, n, k) for _ in range(T)]).astype(np.int32)
+    idx[1, k // 3:] = -1                       # ragged valid count
+    if k > 4:
+        idx[2, 3] = idx[2, 0]                  # duplicate entry
+    idx[4, :] = -1                             # empty query
+    scale = 1 / math.sqrt(576)
+    out, lse, flag = _run(q, kv, idx, scale)
+    assert flag == 0
+    ref, lref = oracle.sparse_mla(q, kv, idx, scale)
+    check_mla(out, lse, ref, lref)
+
+
+def test_distinct_group_scales_and_large_logits():
+    n, T, H, k = 600, 5, 64, 512
+    kv = _rows(n, seed=3, group_scales=True)
+    q = inputs.bf16_bits(inputs.Stream(4).sub("q").normal((T, H, 576), sigma=3.0))  # peaky softmax
+    rng = np.random.default_rng(0)
+    idx = np.stack([rng.permutation(n)[:k] for _ in range(T)]).astype(np.int32)
+    out, lse, flag = _run(q, kv, idx, 0.125)
+    assert flag == 0
+    ref, lref = oracle.sparse_mla(q, kv, idx, 0.125)
+    check_mla(out, lse, ref, lref)
+
+
+def test_paged_logical_indices():
+    w = inputs.config2(seed=31, B=3, lo=300, hi=3000, Hi=8, Di=64, H=64, topk=256)
+    rng = np.random.default_rng(1)
+    idx = np.full((w.T, w.topk), -1, np.int32)
+    for t in range(w.T):
+        n = int(w.token_kvlen[t])
+        sel = np.sort(rng.choice(n, size=min(n, w.topk), replace=False))
+        idx[t, :len(sel)] = sel
+    out, lse, flag = _run(w.q_mla, w.kv_pool, idx, w.softmax_scale, w.block_table, w.token_req)
+    assert flag == 0
+    ref, lref = oracle.sparse_mla(w.q_mla, w.kv_pool, idx, w.softmax_scale, w.block_table, w.token_req)
+    check_mla(out, lse, ref, lref)
+
+
+def test_out_of_range_rows_flagged_and_skipped():
+    kv = _rows(100, seed=5)
+    q = inputs.bf16_bits(inputs.Stream(5).sub("q").normal((2, 8, 576)))
+    idx = np.array([[1, 2, 100, 3], [5, 6, 7, 8]], np.int32)
+    out, lse, flag = _run(q, kv, idx, 0.05)
+    assert flag & 0x01
+    ref, lref = oracle.sparse_mla(q, kv, np.array([[1, 2, -1, 3], [5, 6, 7, 8]], np.int32), 0.05)
+    check_mla(out, lse, ref, lref)
+
+
+def test_host_side_validation():
+    kv = torch.zeros((10, 656), dtype=torch.uint8, device="cuda")
+    q = torch.zeros((1, 65, 576), dtype=torch.bfloat16, device="cuda")
+    idx = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    out = torch.empty((1, 65, 512), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(HSError):
+        hs_sparse_mla_fwd(q, kv, idx, 1.0, out, err)   # H = 65 > 64

@@ -1,0 +1,63 @@
+"""End-to-end parity of one hot-path step (indexer -> top-k -> sparse MLA) on the benchmark's
+workloads: the tiny prefill in full, and the MTP-decode and chunked-prefill workloads at full
+size on sampled query tokens (the oracle computes those tokens one by one)."""
+import numpy as np
+import pytest
+
+import oracle
+from dsa_sparse_mla_gb300 import hs_check_flag, inputs
+from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
+
+from parity import check_mla, check_topk_sets
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_tokens(w, hp, rows):
+    rows = np.asarray(rows)
+    sl = lambda a: np.ascontiguousarray(a[rows])
+    idx_gpu = hp.idx.cpu().numpy()[rows]
+    # the oracle's own scores and top-k for these tokens
+    ref_scores = oracle.indexer_scores(sl(w.q_idx), sl(w.q_scale), sl(w.weights), w.k_cache, w.k_scale, w.block_table,
+                                       sl(w.token_req), sl(w.token_kvlen), ld=w.ld)
+    ref_idx = oracle.topk(ref_scores, sl(w.token_kvlen), w.topk)
+    ndiff = check_topk_sets(idx_gpu, ref_scores, sl(w.token_kvlen), w.topk, ref_idx)
+    # attention checked on the GPU's index set
+    out_ref, lse_ref = oracle.sparse_mla(sl(w.q_mla), w.kv_pool, idx_gpu, w.softmax_scale, w.block_table,
+                                         sl(w.token_req))
+    check_mla(hp.out[rows], hp.lse[rows], out_ref, lse_ref)
+    return ndiff
+
+
+def test_tiny_prefill_full():
+    w = inputs.config1()
+    hp = HotPath(DeviceWorkload.from_host(w))
+    hp.step()
+    assert hs_check_flag(hp.err) == 0
+    _check_tokens(w, hp, np.arange(w.T))
+
+
+def test_mtp_decode_full_size_sampled():
+    w = inputs.config2()
+    hp = HotPath(DeviceWorkload.from_host(w))
+    hp.step()
+    assert hs_check_flag(hp.err) == 0
+    rows = [0, 1, 2, 3, 101, 254, 255]
+    _check_tokens(w, hp, rows)
+
+
+def test_chunked_prefill_full_size_sampled():
+    w = inputs.config3()
+    hp = HotPath(DeviceWorkload.from_host(w))
+    hp.step()
+    assert hs_check_flag(hp.err) == 0
+    _check_tokens(w, hp, [0, 777, 2047])
+
+
+def test_repeat_is_deterministic():
+    w = inputs.config2(seed=41, B=8, lo=3000, hi=9000)
+    hp = HotPath(DeviceWorkload.from_host(w))
+    hp.step()
+    a = (hp.idx.clone(), hp.out.clone(), hp.lse.clone())
+    hp.step()
+    assert hp.idx.equal(a[0]) and hp.out.equal(a[1]) and hp.lse.equal(a[2])

@@ -1,0 +1,62 @@
+"""GPU top-k is bit-exact against the oracle when both rank the same fp32 scores."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dsa_sparse_mla_gb300 import hs_check_flag, hs_topk
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(scores: np.ndarray, kvlen: np.ndarray, k: int) -> np.ndarray:
+    s = torch.from_numpy(np.ascontiguousarray(scores, dtype=np.float32)).cuda()
+    kl = torch.from_numpy(np.ascontiguousarray(kvlen, dtype=np.int32)).cuda()
+    idx = torch.full((scores.shape[0], k), -7, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hs_topk(s, kl, k, idx, err)
+    assert hs_check_flag(err) == 0
+    return idx.cpu().numpy()
+
+
+@pytest.mark.parametrize("ld,k", [(700, 64), (5000, 256), (70000, 2048)])
+def test_random_with_ties_and_short_rows(ld, k):
+    rng = np.random.default_rng(ld)
+    T = 24
+    s = rng.standard_normal((T, ld)).astype(np.float32)
+    s[::2] = np.round(s[::2] * 8) / 8          # heavy ties
+    s[3, :] = 1.0                              # all equal
+    s[5, ::7] = 0.0
+    s[5, 1::7] = -0.0                          # signed zeros tie
+    kvlen = rng.integers(0, ld + 1, size=T).astype(np.int32)
+    kvlen[:5] = [0, 1, k, k + 1, ld]
+    got = _run(s, kvlen, k)
+    ref = oracle.topk(s.astype(np.float64), kvlen, k)
+    assert np.array_equal(got, ref)
+
+
+def test_long_rows_like_long_prefill():
+    rng = np.random.default_rng(7)
+    T, ld, k = 6, 131072, 2048
+    s = (rng.random((T, ld), dtype=np.float32) * 40).astype(np.float32)   # positive, like ReLU sums
+    s[1] = np.float32(3.0)                                                 # one giant tie
+    kvlen = np.array([ld, ld, ld - 1, 65537, 2049, 4096], np.int32)
+    got = _run(s, kvlen, k)
+    ref = oracle.topk(s.astype(np.float64), kvlen, k)
+    assert np.array_equal(got, ref)
+
+
+def test_specials_nan_and_infinities():
+    s = np.array([[np.nan, -np.inf, 3.0, np.nan, np.inf, -0.0, 0.0, 2.0] * 40], np.float32)
+    kvlen = np.array([320], np.int32)
+    for k in (1, 7, 100, 300):
+        assert np.array_equal(_run(s, kvlen, k), oracle.topk(s.astype(np.float64), kvlen, k))
+
+
+def test_bad_length_flagged():
+    s = torch.zeros((2, 100), dtype=torch.float32, device="cuda")
+    kl = torch.tensor([50, 101], dtype=torch.int32, device="cuda")
+    idx = torch.empty((2, 8), dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hs_topk(s, kl, 8, idx, err)
+    assert hs_check_flag(err) & 0x02
