@@ -1,0 +1,420 @@
+"""Benchmark of the sparse-MLA layer hot path on one GB300 (or N, one process per GPU).
+
+One step = one pass of the whole hot path over one batch: hs_indexer_scores -> hs_topk ->
+hs_sparse_mla_fwd, on the MTP-decode batch (64 requests x (1+3) query tokens, contexts
+16K-64K, 64 x 128-d FP8 index heads, top-2048, 64 MLA heads, paged FP8 KV). Prints one JSON
+line. Other workloads (tiny prefill, chunked prefill, long prefill chunks, HiSparse decode) are
+available with --config for analysis; the default line is the MTP-decode one.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2]
+
+Timing: W untimed steps, then K steps; before each timed step a 256 MB buffer is written so L2
+(126 MB) holds nothing of the previous step; each step is bracketed by CUDA events on the
+launching stream; the reported time is the mean per step, max over ranks. Per-kernel events
+inside the timed steps give each kernel's average duration for the roofline. `e2e` repeats the
+step through the same API with the step's inputs copied from pinned host memory and the outputs
+copied back inside the timed region. `cpu_baseline` times the CPU oracle (test
+infrastructure, never on the product path) on a bounded sample of the same workload.
+`--impl reference` times only that oracle, which is the reference implementation here.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA layer tokens/s (indexer+top-k+attn); % of GB300 roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate ratio
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------------ distributed -------
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank decodes its own batch (weak scaling): a distinct, reproducible seed."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------ clocks ------------
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append({"sm": float(f[2]), "max": float(f[3]), "power": float(f[4]),
+                             "hw": f[6], "hwt": f[7], "swt": f[8], "pcap": f[9]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [r for r in rows if r["power"] > 0.5 * max(x["power"] for x in rows)] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy), "power_w_max": max(r["power"] for r in rows)}
+
+
+# ------------------------------------------------------------------------ traffic record -----
+
+def kernel_source_digest(kernel: str) -> str:
+    src = {"indexer": "indexer.cu", "topk": "topk.cu", "mla": "mla.cu", "resolve": "resolve.cu"}[kernel]
+    h = hashlib.sha256()
+    for f in (src, "common.cuh"):
+        with open(os.path.join(ROOT, "dsa_sparse_mla_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on this workload,
+    or None if there is none or the kernel's source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "%s.%s.md" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_source_digest(kernel):
+        return None
+    return float(m.group(1))
+
+
+# ------------------------------------------------------------------------ workloads ---------
+
+def build_workload(config: int, seed: int, requests: int = 64):
+    from dsa_sparse_mla_gb300 import inputs
+    if config == 1:
+        return inputs.config1(seed=seed)
+    if config == 2:
+        return inputs.config2(seed=seed, B=requests)
+    if config == 3:
+        return inputs.config3(seed=seed)
+    raise SystemExit("--config %d: use 1, 2 or 3 for the indexer/top-k/MLA step" % config)
+
+
+def work_of(w):
+    from dsa_sparse_mla_gb300 import costmodel as cm
+    kvsum = int(w.token_kvlen.astype(np.int64).sum())
+    ctxsum = int(w.ctx.astype(np.int64).sum())
+    rows = int(np.minimum(w.token_kvlen, w.topk).astype(np.int64).sum())
+    return {"indexer": cm.indexer_work(w.Hi, w.Di, kvsum, ctxsum, w.T), "topk": cm.topk_work(kvsum, w.T, w.topk),
+            "mla": cm.mla_work(w.H, rows, w.T)}
+
+
+# ------------------------------------------------------------------------ CPU oracle ---------
+
+def oracle_sample(w, tokens, threads=0):
+    """Runs the CPU oracle (indexer -> top-k -> sparse MLA) on the given query tokens; returns
+    the wall time in seconds."""
+    import oracle
+    rows = np.asarray(tokens)
+    sl = lambda a: np.ascontiguousarray(a[rows])
+    t0 = time.perf_counter()
+    s = oracle.indexer_scores(sl(w.q_idx), sl(w.q_scale), sl(w.weights), w.k_cache, w.k_scale, w.block_table,
+                              sl(w.token_req), sl(w.token_kvlen), ld=w.ld, threads=threads)
+    idx = oracle.topk(s, sl(w.token_kvlen), w.topk, threads=threads)
+    oracle.sparse_mla(sl(w.q_mla), w.kv_pool, idx, w.softmax_scale, w.block_table, sl(w.token_req), threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------------------ GPU arm -----------
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import dsa_sparse_mla_gb300 as hs
+    from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
+
+    hs.load()
+    peaks, peaks_kind = load_peaks()
+    w = build_workload(args.config, rank_seed(args.config, rank), args.requests)
+    dw = DeviceWorkload.from_host(w, dev)
+    hp = HotPath(dw)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    work = work_of(w)
+
+    for _ in range(args.warmup):
+        hp.step()
+    torch.cuda.synchronize()
+    if hs.hs_check_flag(hp.err):
+        raise SystemExit("device error flag set during warm-up: 0x%x" % hs.hs_check_flag(hp.err))
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e = ev[i]
+        e[0].record(stream)
+        hp.indexer()
+        e[1].record(stream)
+        hp.topk()
+        e[2].record(stream)
+        hp.mla()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
+    t_idx = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    t_mla = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    ms_step = max_over_ranks(float(np.mean(t_step)), world, dev)
+    flag = hs.hs_check_flag(hp.err)
+
+    # ---- end to end through host buffers (pinned), same API
+    pin = lambda t: t.cpu().pin_memory()
+    h_in = [pin(dw.q_idx), pin(dw.q_scale), pin(dw.weights), pin(dw.q_mla), pin(dw.token_req), pin(dw.token_kvlen)]
+    d_in = [dw.q_idx, dw.q_scale, dw.weights, dw.q_mla, dw.token_req, dw.token_kvlen]
+    h_out = [torch.empty_like(hp.out, device="cpu").pin_memory(), torch.empty_like(hp.lse, device="cpu").pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    K2 = max(1, min(K, 200))
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K2)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K2):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        hp.step()
+        h_out[0].copy_(hp.out, non_blocking=True)
+        h_out[1].copy_(hp.lse, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in e2e_ev])), world, dev)
+    clk = clocks.stop() if rank == 0 else None
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    tokens = w.T * world
+    ms = {"indexer": float(np.mean(t_idx)), "topk": float(np.mean(t_topk)), "mla": float(np.mean(t_mla))}
+    hbm = float(peaks["hbm_gbs"])
+    fp8 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * FP8_PER_BF16
+    bf16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    kern = {}
+    for name in ("indexer", "topk", "mla"):
+        wk = work[name]
+        t = ms[name] * 1e-3
+        gbs = wk.bytes / t / 1e9
+        tf = wk.flops / t / 1e12
+        t_roof = max(wk.bytes / (hbm * 1e9), wk.flops / ((fp8 if name == "indexer" else bf16) * 1e12))
+        kern[name] = {"ms": round(ms[name], 4), "share": None, "bytes": wk.bytes, "flops": wk.flops,
+                      "gbs": round(gbs, 1), "tflops": round(tf, 1), "roofline_ms": round(t_roof * 1e3, 4),
+                      "roofline_frac": round(t_roof / t, 4)}
+    tot = sum(ms.values())
+    for name in kern:
+        kern[name]["share"] = round(ms[name] / tot, 4)
+    dom = max(ms, key=ms.get)
+    wk = work[dom]
+    t_dom = ms[dom] * 1e-3
+    bytes_bound = wk.bytes / (hbm * 1e9) >= wk.flops / ((fp8 if dom == "indexer" else bf16) * 1e12)
+    if bytes_bound:
+        roof = {"bound": "hbm", "achieved": round(wk.bytes / t_dom / 1e9, 1), "peak": hbm, "unit": "GB/s"}
+    else:
+        pk = fp8 if dom == "indexer" else bf16
+        roof = {"bound": "tensor", "achieved": round(wk.flops / t_dom / 1e12, 1), "peak": pk, "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["kernel"] = dom
+    roof["peak_source"] = ("%s (MEASURED_PEAKS.json)" % peaks_kind) + (
+        "; fp8 = sustained bf16 x nominal 2" if (dom == "indexer" and not bytes_bound) else "")
+    roof["traffic"] = recorded_traffic(dom, w.name)
+    layer_roof_ms = sum(kern[n]["roofline_ms"] for n in kern)
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.num_threads(0)
+        sample = list(range(min(w.T, max(4, threads))))
+        wall_cpu = oracle_sample(w, sample, threads=0)
+        cpu = {"value": round(len(sample) / wall_cpu, 3), "unit": "tokens/s", "cores": min(threads, len(sample)),
+               "kind": "oracle", "sample": "%d query tokens of the same batch (first %d requests), full "
+               "indexer+top-k+MLA in float64; %.1f s wall on %s" % (len(sample), len(sample) // 4 or 1, wall_cpu,
+                                                                     cpu_model())}
+
+    line = {"metric": METRIC, "value": round(tokens / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
+            "config": {"workload": w.name, "requests": w.B, "query_tokens": w.T, "ctx": "U{16384..65536}",
+                       "index_heads": w.Hi, "index_dim": w.Di, "topk": w.topk, "mla_heads": w.H, "page": 64,
+                       "l2": "256 MB write between timed steps (inputs also > L2)", "parallelism": "dp%d" % world},
+            "roofline": roof,
+            "layer_roofline_frac": round(layer_roof_ms / tot, 4),
+            "kernels": kern,
+            "e2e": {"value": round(tokens / (ms_e2e * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4), "steps": K2},
+            "gpu_launches": 3 * K, "cpu_baseline": cpu, "clocks": clk, "wall_s_timed_region": round(wall, 3),
+            "device_flag": flag}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------ reference arm -----
+
+def run_reference(args):
+    """The CPU oracle timed as the reference implementation, on the same workload and metric."""
+    rank, world, local = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads(0)
+    w = build_workload(args.config, rank_seed(args.config, 0), args.requests)
+    per_step = max(4, threads)              # query tokens per step: one token per core
+    # size the sample so that warm-up + timed steps stay within about three minutes
+    probe = oracle_sample(w, list(range(per_step)), threads=0)
+    budget = 180.0
+    steps_timed = max(1, min(args.steps, int(budget / max(probe, 1e-3)) - args.warmup))
+    for i in range(min(args.warmup, 1)):
+        oracle_sample(w, list(range(per_step)), threads=0)
+    t = 0.0
+    ntok = 0
+    for i in range(steps_timed):
+        start = (i * per_step) % w.T
+        toks = [(start + j) % w.T for j in range(per_step)]
+        t += oracle_sample(w, toks, threads=0)
+        ntok += len(toks)
+    value = ntok / t
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "steps_timed": steps_timed, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / steps_timed, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "query_tokens_per_step": per_step},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle", "cores": threads,
+                             "sample": "%d query tokens per step (indexer+top-k+MLA, float64) of %s, %d timed steps "
+                                       "on %s" % (per_step, w.name, steps_timed, cpu_model())},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--requests", type=int, default=64, help="decode batch size (profiling runs use fewer)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -26,6 +26,7 @@ constexpr int kStages = 6;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxG = 32;      // tokens per group when Hi = 8
+constexpr int kMaxTpc = 64;    // tiles per CTA and segment
 
 struct Params {
   int32_t T, B, Hi, Di;
@@ -56,7 +57,8 @@ struct Cfg {
   static constexpr int kOffW = kOffK + kStages * kTileBytes;
   static constexpr int kOffTok = kOffW + kN * 4;              // int32 x 4 x kMaxG
   static constexpr int kOffSeg = kOffTok + 4 * kMaxG * 4;     // int32 x 4 x kMaxG
-  static constexpr int kOffBar = kOffSeg + 4 * kMaxG * 4;
+  static constexpr int kOffBlk = kOffSeg + 4 * kMaxG * 4;   // int32 [kMaxG][2 * kMaxTpc]
+  static constexpr int kOffBar = kOffBlk + kMaxG * 2 * kMaxTpc * 4;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 64 + 1024;          // + alignment slack
@@ -79,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* sSegN = sSegReq + kMaxG;                      // max visible keys in the segment
   int32_t* sSegLo = sSegN + kMaxG;                       // first tile of this CTA
   int32_t* sSegHi = sSegLo + kMaxG;                      // one past the last tile
+  int32_t* sBlk = (int32_t*)(smem + C::kOffBlk);         // physical page of each of the CTA's pages
   uint64_t* bars = (uint64_t*)(smem + C::kOffBar);
   uint64_t* full = bars;                                 // [kStages]
   uint64_t* empty = bars + kStages;                      // [kStages]
@@ -114,8 +117,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sTokSeg[tid] = (n > 0) ? r : -1;  // request for now; turned into a segment id below
   }
   if (tid < G * HI) {
+    // folded weight w * q_scale; heads 4m+2, 4m+3 take their ReLU as x + |x| = 2 max(x, 0), so
+    // their weight carries the factor 1/2 (exact)
     const int g = tid / HI, h = tid % HI, t = t0 + g;
-    sW[tid] = (t < p.T) ? p.weights[(int64_t)t * HI + h] * p.q_scale[(int64_t)t * HI + h] : 0.f;
+    const float half = (h & 2) ? 0.5f : 1.f;
+    sW[tid] = (t < p.T) ? half * (p.weights[(int64_t)t * HI + h] * p.q_scale[(int64_t)t * HI + h]) : 0.f;
   }
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -159,6 +165,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = nseg;
   }
   __syncthreads();
+  // stage this CTA's block-table entries (2 pages per tile) so no warp waits on them later
+  for (int s = 0; s < misc[0]; ++s) {
+    const int r = sSegReq[s];
+    const int npg = 2 * (sSegHi[s] - sSegLo[s]);
+    for (int i = tid; i < npg; i += kThreads) {
+      const int page = 2 * sSegLo[s] + i;
+      int32_t b = -1;
+      if (page * 64 < sSegN[s]) {
+        b = p.block_table[(int64_t)r * p.bt_stride + page];
+        if (b < 0 || (int64_t)b >= p.nblk) {
+          flag_error(p.err, HS_FLAG_BAD_BLOCK);
+          b = -1;
+        }
+      }
+      sBlk[s * 2 * kMaxTpc + i] = b;
+    }
+  }
+  __syncthreads();
   tc_fence_after();
   const int nseg = misc[0];
   const uint32_t tmem = (uint32_t)misc[2];
@@ -175,7 +199,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(sQ, &map_q, q_full, 0, t0 * HI);
         int it = 0;
         for (int s = 0; s < nseg && !*abort_flag; ++s) {
-          const int r = sSegReq[s];
           for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
             const int st = it % kStages;
             const uint32_t ph = (uint32_t)(it / kStages) & 1u;
@@ -186,17 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t blk[2];
             uint32_t bytes = 0;
             for (int pg = 0; pg < 2; ++pg) {
-              const int page = 2 * kt + pg;
-              blk[pg] = -1;
-              if (page * 64 < sSegN[s]) {
-                const int32_t b = p.block_table[(int64_t)r * p.bt_stride + page];
-                if (b >= 0 && (int64_t)b < p.nblk) {
-                  blk[pg] = b;
-                  bytes += 64 * DI;
-                } else {
-                  flag_error(p.err, HS_FLAG_BAD_BLOCK);
-                }
-              }
+              blk[pg] = sBlk[s * 2 * kMaxTpc + 2 * (kt - sSegLo[s]) + pg];
+              if (blk[pg] >= 0) bytes += 64 * DI;
             }
             mbar_arrive_expect_tx(&full[st], bytes);
             for (int pg = 0; pg < 2; ++pg)
@@ -246,61 +260,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // ------------------------------------------------------------ epilogue --------------------
       const int quad = warp & 3;
-      const int half = (warp - 2) >> 2;
+      const int half = (warp - 2) >> 2;  // which half of the 256 columns
       const int row = quad * 32 + lane;
-      int it = 0;
-      bool run = true;
-      for (int s = 0; s < nseg && run; ++s) {
-        const int r = sSegReq[s];
-        const int segn = sSegN[s];
-        for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
-          const int b = it & 1;
-          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-          const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
-          if (!__all_sync(0xffffffffu, go)) {
-            *abort_flag = 1;
-            run = false;
-            break;
-          }
-          tc_fence_after();
-          const int64_t j = (int64_t)kt * kBlockM + row;
-          float ks = 0.f;
-          bool key_ok = false;
-          if (j < segn) {
-            const int32_t blk = p.block_table[(int64_t)r * p.bt_stride + (j >> 6)];
-            if (blk >= 0 && (int64_t)blk < p.nblk) {
-              ks = p.k_scale[(int64_t)blk * 64 + (j & 63)];
-              key_ok = true;
-            }
-          }
-#pragma unroll 1
-          for (int gi = 0; gi < G / 2; ++gi) {
-            const int g = half * (G / 2) + gi;
-            if (sTokSeg[g] != s) continue;  // warp-uniform
-            uint32_t acc[HI];
-            const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kN + g * HI);
-            if constexpr (HI >= 32) {
-#pragma unroll
-              for (int c = 0; c < HI; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
-            } else {
-#pragma unroll
-              for (int c = 0; c < HI; c += 8) tmem_ld8(taddr + c, *reinterpret_cast<uint32_t(*)[8]>(&acc[c]));
-            }
-            tmem_wait_ld();
-            const float* w = sW + g * HI;
-            float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-            for (int h = 0; h < HI; h += 2) {
-              const float2 wv = *reinterpret_cast<const float2*>(w + h);
-              s0 = fmaf(wv.x, fmaxf(__uint_as_float(acc[h]), 0.f), s0);
-              s1 = fmaf(wv.y, fmaxf(__uint_as_float(acc[h + 1]), 0.f), s1);
-            }
-            if (key_ok && j < sTokN[g]) p.scores[(int64_t)(t0 + g) * p.ld + j] = ks * (s0 + s1);
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[b]);
+      // key scale of this thread's key in item (s, kt); < 0 marks a key outside the request
+      auto key_scale = [&](int s, int kt) -> float {
+        const int64_t j = (int64_t)kt * kBlockM + row;
+        if (j >= sSegN[s]) return -1.f;
+        const int32_t blk = sBlk[s * 2 * kMaxTpc + 2 * (kt - sSegLo[s]) + (row >> 6)];
+        return blk >= 0 ? __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63)) : -1.f;
+      };
+      int s = 0;
+      while (s < nseg && sSegHi[s] <= sSegLo[s]) ++s;
+      int kt = s < nseg ? sSegLo[s] : 0;
+      float ks = s < nseg ? key_scale(s, kt) : -1.f;
+      for (int it = 0; it < total; ++it) {
+        // next item, and its key scale fetched before waiting (its latency overlaps this tile)
+        int s2 = s, kt2 = kt + 1;
+        while (s2 < nseg && kt2 >= sSegHi[s2]) {
+          ++s2;
+          kt2 = s2 < nseg ? sSegLo[s2] : 0;
         }
+        const float ks2 = s2 < nseg ? key_scale(s2, kt2) : -1.f;
+        const int b = it & 1;
+        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
+        if (!__all_sync(0xffffffffu, go)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const int64_t j = (int64_t)kt * kBlockM + row;
+        const bool key_ok = ks >= 0.f;
+#pragma unroll 1
+        for (int gi = 0; gi < G / 2; ++gi) {
+          const int g = half * (G / 2) + gi;
+          if (sTokSeg[g] != s) continue;  // warp-uniform
+          uint32_t acc[HI];
+          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kN + g * HI);
+          if constexpr (HI >= 32) {
+#pragma unroll
+            for (int c = 0; c < HI; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
+          } else {
+#pragma unroll
+            for (int c = 0; c < HI; c += 8) tmem_ld8(taddr + c, *reinterpret_cast<uint32_t(*)[8]>(&acc[c]));
+          }
+          tmem_wait_ld();
+          // sum_h w'[h] * relu(dot[h]): half the ReLUs on the ALU pipe (max), half on the FMA
+          // pipe (x + |x|), products accumulated with packed fp32x2 FMAs
+          const float* w = sW + g * HI;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int h = 0; h < HI; h += 4) {
+            const float4 wv = *reinterpret_cast<const float4*>(w + h);
+            const float x0 = __uint_as_float(acc[h]), x1 = __uint_as_float(acc[h + 1]);
+            const float x2 = __uint_as_float(acc[h + 2]), x3 = __uint_as_float(acc[h + 3]);
+            ffma2(s0, s1, fmaxf(x0, 0.f), fmaxf(x1, 0.f), wv.x, wv.y);
+            ffma2(s2, s3, x2 + fabsf(x2), x3 + fabsf(x3), wv.z, wv.w);
+          }
+          if (key_ok && j < sTokN[g]) p.scores[(int64_t)(t0 + g) * p.ld + j] = ks * ((s0 + s1) + (s2 + s3));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        s = s2;
+        kt = kt2;
+        ks = ks2;
       }
     }
   }

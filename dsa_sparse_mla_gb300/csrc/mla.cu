@@ -7,16 +7,21 @@
 //   logit_i = scale * <q[t,h,:], [latent_i, rope_i]>,  out = softmax(logit) . latent,  lse = ln sum exp.
 //
 // One CTA per query token (416 threads):
-//   warps 0-7   gather 64 rows per tile (thread = one row x one 128-element scale group), with
-//               16-byte loads, dequantise latent = e4m3 * group scale to bf16 and write it, with
-//               the bf16 RoPE part, into a 128-byte-swizzled [dim block][row] tile (2 stages);
-//   warp 8      allocates TMEM and issues the MMAs:
-//                 S   = Q . K^T        M = 64 heads, N = 64 rows, K = 576  (A = Q, B = tile)
-//                 O^T += V^T . P^T     M = 128 dims (x4), N = 64 heads, K = 64 rows
-//               The same tile serves as the K-major B of the first and, read MN-major, as the A of
-//               the second, so it is dequantised once;
-//   warps 9-12  online softmax: each of the 64 head threads owns one row of S (thread-local max
-//               and sum); P goes to shared memory as bf16. O^T lives in TMEM and is rescaled only
+//   warps 0-7   gather 64 rows per tile (a warp per row at a time, 16-byte coalesced loads),
+//               dequantise latent = e4m3 * group scale to fp16 (exact e4m3 -> fp16 conversion, one
+//               rounding for the scale) and write it, with the bf16 RoPE part as stored, into a
+//               128-byte-swizzled [dim block][row] tile (2 stages);
+//   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 64 rows,
+//               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile and an S
+//               buffer are ready;
+//   warp 9      issues O^T += V^T . P^T (M = 128 dims x4, N = 64 heads, K = 64 rows) as soon as P is
+//               ready. Two issuers keep QK of the next tiles from queueing behind PV of the current
+//               one. The same tile is the K-major B of QK and, read MN-major, the A of PV, so it is
+//               dequantised once. Producers load and dequantise the next tile into registers
+//               while they wait for a free stage, so global-memory latency is off the MMA chain;
+//   warps 10-13 first convert Q's latent dims to fp16 in shared memory, then run the online
+//               softmax: two threads share each head's row of S (one shuffle for the max); P goes to
+//               shared memory as fp16. O^T lives in TMEM and is rescaled only
 //               when a head's running max grows by more than 2^8 (lazy rescaling); the final pass
 //               divides by the row sum and writes bf16.
 // TMEM: columns 0-127 hold two S buffers (64-row layout), 128-383 hold O^T.
@@ -27,9 +32,10 @@ namespace mla {
 
 constexpr int kRows = 64;
 constexpr int kProdWarps = 8;
-constexpr int kMmaWarp = kProdWarps;
+constexpr int kMmaWarp = kProdWarps;       // QK issuer; also allocates TMEM
+constexpr int kPvWarp = kProdWarps + 1;    // PV issuer
 constexpr int kSmThreads = 128;
-constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
+constexpr int kThreads = 32 * (kProdWarps + 2 + 4);
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
 constexpr int kBlk = 8192;                 // one [64 rows][128 B] swizzled block
@@ -42,12 +48,15 @@ constexpr int kOffP = kOffStage + 2 * kStageBytes;
 constexpr int kOffValid = kOffP + kPBytes;          // uint8 [2][64]
 constexpr int kOffAlpha = kOffValid + 128;          // float [64]
 constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
-constexpr int kOffBar = kOffInvL + 256;             // 12 barriers
-constexpr int kOffMisc = kOffBar + 12 * 8;          // tmem base, abort
+constexpr int kOffBar = kOffInvL + 256;             // 14 barriers
+constexpr int kOffMisc = kOffBar + 14 * 8;          // tmem base, abort
 constexpr int kSmem = kOffMisc + 16 + 1024;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kF16Max = 65504.f;
+constexpr float kScaleMax = 65504.f / 448.f;     // |code * scale| stays finite in fp16
+constexpr float kScaleMin = 6.103515625e-05f;    // 2^-14: scales stay fp16 normals
 
 struct Params {
   int32_t T, H, k;
@@ -63,11 +72,17 @@ struct Params {
   int32_t* err;
 };
 
-__device__ __forceinline__ uint32_t dequant2(uint16_t codes, float scale) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)codes, __NV_E4M3);
-  float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
-  __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-  return *reinterpret_cast<uint32_t*>(&b);
+// 8 e4m3 codes (two 32-bit words) -> 8 fp16 values code * scale: the e4m3 -> fp16 conversion is
+// exact, the packed multiply rounds once.
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t w0, uint32_t w1, uint32_t scale2) {
+  uint4 r;
+  asm("{ .reg .b16 a, b, c, d; .reg .b32 x, y, z, u;\n"
+      " mov.b32 {a, b}, %4; mov.b32 {c, d}, %5;\n"
+      " cvt.rn.f16x2.e4m3x2 x, a; cvt.rn.f16x2.e4m3x2 y, b; cvt.rn.f16x2.e4m3x2 z, c; cvt.rn.f16x2.e4m3x2 u, d;\n"
+      " mul.rn.f16x2 %0, x, %6; mul.rn.f16x2 %1, y, %6; mul.rn.f16x2 %2, z, %6; mul.rn.f16x2 %3, u, %6; }"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "r"(w0), "r"(w1), "r"(scale2));
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -88,7 +103,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_ready = bars + 8;   // softmax wrote P (and corrected O) -> MMA
   uint64_t* pv_done = bars + 9;   // PV done -> softmax
   uint64_t* q_full = bars + 10;
-  uint64_t* mma_done = bars + 11;
+  uint64_t* mma_done = bars + 11;  // QK issuer's MMAs drained
+  uint64_t* pv_drain = bars + 12;  // PV issuer's MMAs drained
+  uint64_t* q_ready = bars + 13;   // Q converted to fp16 (latent dims) -> QK issuer
   uint32_t* misc = (uint32_t*)(smem + kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -108,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(pv_done, 1);
     mbar_init(q_full, 1);
     mbar_init(mma_done, 1);
+    mbar_init(pv_drain, 1);
+    mbar_init(q_ready, 4);
     mbar_fence_init();
     misc[1] = 0;
   }
@@ -118,91 +137,166 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProdWarps) {
     // ================================================================ gather + dequantise ======
-    const int row = tid >> 2;   // 0..63
-    const int grp = tid & 3;    // 128-element scale group
+    // Warp w owns rows 8w .. 8w+7 of every tile. For one row, lane j loads latent bytes
+    // [16j, 16j+16) (the whole 512-byte latent in one coalesced instruction), lanes 0-3 the four
+    // group scales and lanes 4-11 the 128-byte RoPE part. Software pipeline per warp:
+    //   tile i+4: index entries (lanes 0-7)     tile i+3: block-table entries
+    //   tile i+2: rows prefetched into L2 by the TMA engine (one 656-byte bulk prefetch per row)
+    //   tile i+1: row data loaded into registers
+    //   tile i  : dequantised into its stage once the stage is free.
+    // Loads are volatile so they are issued here and not next to their first use.
     const int req = p.bt ? p.token_req[t] : 0;
-    for (int i = 0; i < ntiles; ++i) {
+    const int64_t idx_base = (int64_t)t * k;
+    auto ld_idx = [&](int i) -> int32_t {  // lane rr < 8: index entry of row 8 * warp + rr of tile i
+      const int e = i * kRows + warp * 8 + lane;
+      return (lane < 8 && i < ntiles && e < k) ? ldg_nc_s32(p.idx + idx_base + e) : -1;
+    };
+    auto ld_blk = [&](int32_t j) -> int32_t {  // lanes 0-7: block-table entry of entry j (j itself if none)
+      if (lane >= 8 || j < 0 || !p.bt) return j;
+      const int32_t page = j >> 6;
+      return page < p.bt_stride ? ldg_nc_s32(p.bt + (int64_t)req * p.bt_stride + page) : -1;
+    };
+    auto phys_row = [&](int32_t j, int32_t b) -> int64_t {  // lanes 0-7: physical row, -1 if none
+      if (lane >= 8 || j < 0) return -1;
+      const int64_t r = p.bt ? (b >= 0 ? (int64_t)b * 64 + (j & 63) : -1) : (int64_t)j;
+      if (r < 0 || r >= p.R) {
+        flag_error(p.err, HS_FLAG_BAD_INDEX);
+        return -1;
+      }
+      return r;
+    };
+    uint4 lat[8], rope[8];     // row data of the next tile: latent (all lanes), RoPE (lanes 4-11)
+    float scl[8];              // lanes 0-3: group scale (lane) of each row
+    int64_t my_row = -1;       // lanes 0-7: physical row of the tile whose data is loaded
+    auto ld_rows = [&](int64_t rows_lane) {
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr) {
+        const int64_t r = __shfl_sync(0xffffffffu, rows_lane, rr);
+        lat[rr] = make_uint4(0, 0, 0, 0);
+        rope[rr] = make_uint4(0, 0, 0, 0);
+        scl[rr] = 0.f;
+        if (r >= 0) {
+          const uint8_t* src = p.kv + r * HS_KV_ROW_BYTES;
+          lat[rr] = ldg_nc_v4(src + 16 * lane);
+          if (lane < 4) scl[rr] = ldg_nc_f32(src + HS_D_LATENT + 4 * lane);
+          else if (lane < 12) rope[rr] = ldg_nc_v4(src + HS_D_LATENT + 16 + 16 * (lane - 4));
+        }
+      }
+    };
+    // waits for stage i % 2, dequantises the loaded rows into it and publishes it; false on abort
+    auto publish = [&](int i) -> bool {
       const int s = i & 1;
       int go = 1;
       if (lane == 0) go = !*abort_flag && mbar_wait(&empty[s], ((uint32_t)(i >> 1) & 1u) ^ 1u, p.err);
       if (!__shfl_sync(0xffffffffu, go, 0)) {
         if (lane == 0) *abort_flag = 1;
-        break;
-      }
-      const int e = i * kRows + row;
-      bool valid = false;
-      int64_t prow = 0;
-      if (e < k) {
-        const int32_t j = p.idx[(int64_t)t * k + e];
-        if (j >= 0) {
-          if (p.bt) {
-            const int32_t page = j >> 6;
-            int32_t blk = -1;
-            if (page < p.bt_stride) blk = p.bt[(int64_t)req * p.bt_stride + page];
-            prow = (int64_t)blk * 64 + (j & 63);
-            valid = blk >= 0 && prow < p.R;
-          } else {
-            prow = j;
-            valid = prow < p.R;
-          }
-          if (!valid && grp == 0) flag_error(p.err, HS_FLAG_BAD_INDEX);
-        }
-      }
-      uint4 lat[8], rope[2];
-      float scale = 0.f;
-      if (valid) {
-        const uint8_t* src = p.kv + prow * HS_KV_ROW_BYTES;
-        const uint4* l4 = reinterpret_cast<const uint4*>(src + grp * 128);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) lat[c] = __ldg(l4 + c);
-        scale = __ldg(reinterpret_cast<const float*>(src + HS_D_LATENT) + grp);
-        const uint4* r4 = reinterpret_cast<const uint4*>(src + HS_D_LATENT + 16);
-        rope[0] = __ldg(r4 + 2 * grp);
-        rope[1] = __ldg(r4 + 2 * grp + 1);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) lat[c] = make_uint4(0, 0, 0, 0);
-        rope[0] = rope[1] = make_uint4(0, 0, 0, 0);
+        return false;
       }
       uint8_t* st = sStage + s * kStageBytes;
+      uint8_t* blk = st + (lane >> 2) * kBlk;  // dim block of dims 16 * lane .. +15
+      const int ch0 = (lane & 3) * 2;
+      const int first = (lane >> 2) & 1;    // store order alternates so a store hits 8 bank groups
+      bool range_ok = true;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        // 16 latent dims grp*128 + c*16 .. +15 -> dim block 2*grp + c/4, 16-byte chunks 2*(c%4), +1
-        uint8_t* blk = st + (2 * grp + (c >> 2)) * kBlk;
-        const int ch = (c & 3) * 2;
-        uint4 lo, hi;
-        lo.x = dequant2((uint16_t)(lat[c].x & 0xFFFF), scale);
-        lo.y = dequant2((uint16_t)(lat[c].x >> 16), scale);
-        lo.z = dequant2((uint16_t)(lat[c].y & 0xFFFF), scale);
-        lo.w = dequant2((uint16_t)(lat[c].y >> 16), scale);
-        hi.x = dequant2((uint16_t)(lat[c].z & 0xFFFF), scale);
-        hi.y = dequant2((uint16_t)(lat[c].z >> 16), scale);
-        hi.z = dequant2((uint16_t)(lat[c].w & 0xFFFF), scale);
-        hi.w = dequant2((uint16_t)(lat[c].w >> 16), scale);
-        *reinterpret_cast<uint4*>(blk + sw128_offset(row, ch * 16)) = lo;
-        *reinterpret_cast<uint4*>(blk + sw128_offset(row, ch * 16 + 16)) = hi;
+      for (int rr = 0; rr < 8; ++rr) {
+        const int row = warp * 8 + rr;
+        const float scale = __shfl_sync(0xffffffffu, scl[rr], lane >> 3);
+        range_ok &= scale == 0.f || (fabsf(scale) >= kScaleMin && fabsf(scale) <= kScaleMax);
+        const __half2 s2 = __float2half2_rn(scale);
+        const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
+        const uint4 v = lat[rr];
+        const uint4 lo = dequant8_f16(v.x, v.y, s2u);
+        const uint4 hi = dequant8_f16(v.z, v.w, s2u);
+        *reinterpret_cast<uint4*>(blk + sw128_offset(row, (ch0 + first) * 16)) = first ? hi : lo;
+        *reinterpret_cast<uint4*>(blk + sw128_offset(row, (ch0 + 1 - first) * 16)) = first ? lo : hi;
+        if (lane >= 4 && lane < 12)  // RoPE piece lane-4 -> dim block 8, kept in bf16
+          *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(row, (lane - 4) * 16)) = rope[rr];
       }
-      uint8_t* rb = st + 8 * kBlk;
-      *reinterpret_cast<uint4*>(rb + sw128_offset(row, (2 * grp) * 16)) = rope[0];
-      *reinterpret_cast<uint4*>(rb + sw128_offset(row, (2 * grp + 1) * 16)) = rope[1];
-      if (grp == 0) sValid[s * kRows + row] = valid ? 1 : 0;
+      if (!range_ok) flag_error(p.err, HS_FLAG_RANGE);
+      if (lane < 8) sValid[s * kRows + warp * 8 + lane] = my_row >= 0 ? 1 : 0;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[s]);
+      return true;
+    };
+    // prologue: tile 0 in registers, tile 1 prefetched into L2, tile 2 block entries and tile 3
+    // index entries in flight
+    {
+      const int32_t j0 = ld_idx(0);
+      my_row = phys_row(j0, ld_blk(j0));
+    }
+    ld_rows(my_row);
+    int64_t row_next;  // lanes 0-7: physical row of tile i+1 (already prefetched)
+    {
+      const int32_t j1 = ld_idx(1);
+      row_next = phys_row(j1, ld_blk(j1));
+      if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
+    }
+    int32_t jA = ld_idx(2);
+    int32_t bA = ld_blk(jA);
+    int32_t jB = ld_idx(3);
+    for (int i = 0; i < ntiles; ++i) {
+      if (!publish(i)) break;
+      // advance: tile i+1 into registers (from L2), tile i+2 into L2, tile i+3 block entries,
+      // tile i+4 index entries
+      my_row = row_next;
+      ld_rows(my_row);
+      row_next = phys_row(jA, bA);
+      if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
+      jA = jB;
+      bA = ld_blk(jB);
+      jB = ld_idx(i + 4);
     }
   } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer ================
+    // ================================================================ QK issuer =================
     if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(64, kRows, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_bf16(128, 64, 1, 0);
+      constexpr uint32_t idesc_qk = idesc_f16(64, kRows, 0, 0);       // latent dims: fp16
+      constexpr uint32_t idesc_qk_rope = idesc_bf16(64, kRows, 0, 0); // RoPE dims: bf16
       prefetch_tensormap(&map_q);
       mbar_arrive_expect_tx(q_full, kQBytes);
 #pragma unroll 1
       for (int db = 0; db < 9; ++db) tma_load_2d(sQ + db * kBlk, &map_q, q_full, db * 64, t * p.H);
-      const uint32_t q_addr = smem_u32(sQ), st_addr = smem_u32(sStage), p_addr = smem_u32(sP);
-      bool ok = mbar_wait(q_full, 0, p.err);
-      auto issue_pv = [&](int j) -> bool {
-        if (!mbar_wait(p_ready, (uint32_t)j & 1u, p.err)) return false;
+      const uint32_t q_addr = smem_u32(sQ), st_addr = smem_u32(sStage);
+      bool ok = mbar_wait(q_ready, 0, p.err);
+#pragma unroll 1
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int s = i & 1;
+        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+        if (*abort_flag || !mbar_wait(&full[s], ph, p.err) || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
+        const uint32_t d = tmem + kColS + 64 * s;
+#pragma unroll
+        for (int db = 0; db < 9; ++db) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = smem_desc(q_addr + db * kBlk + kk * 32, 16, 1024, 2);
+            const uint64_t b = smem_desc(sa + db * kBlk + kk * 32, 16, 1024, 2);
+            mma_bf16_ss(d, a, b, db < 8 ? idesc_qk : idesc_qk_rope, (db | kk) != 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&s_full[s]);
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, p.err);
+      mbar_wait(q_full, 0, p.err);
+    }
+  } else if (warp == kPvWarp) {
+    // ================================================================ PV issuer =================
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
+      const uint32_t st_addr = smem_u32(sStage), p_addr = smem_u32(sP);
+      bool ok = true;
+#pragma unroll 1
+      for (int j = 0; j < ntiles; ++j) {
+        if (*abort_flag || !mbar_wait(p_ready, (uint32_t)j & 1u, p.err)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sa = st_addr + (uint32_t)((j & 1) * kStageBytes);
 #pragma unroll
@@ -216,47 +310,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(pv_done);
         mma_commit(&empty[j & 1]);
-        return true;
-      };
-#pragma unroll 1
-      for (int i = 0; i < ntiles && ok; ++i) {
-        const int s = i & 1;
-        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-        if (!mbar_wait(&full[s], ph, p.err) || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
-        const uint32_t d = tmem + kColS + 64 * s;
-#pragma unroll
-        for (int db = 0; db < 9; ++db) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = smem_desc(q_addr + db * kBlk + kk * 32, 16, 1024, 2);
-            const uint64_t b = smem_desc(sa + db * kBlk + kk * 32, 16, 1024, 2);
-            mma_bf16_ss(d, a, b, idesc_qk, (db | kk) != 0 ? 1u : 0u);
-          }
-        }
-        mma_commit(&s_full[s]);
-        if (i >= 1 && !issue_pv(i - 1)) {
-          ok = false;
-          break;
-        }
       }
-      if (ok && ntiles > 0) ok = issue_pv(ntiles - 1);
       if (!ok) *abort_flag = 1;
-      mma_commit(mma_done);
-      mbar_wait(mma_done, 0, p.err);
-      mbar_wait(q_full, 0, p.err);
+      mma_commit(pv_drain);
+      mbar_wait(pv_drain, 0, p.err);
     }
   } else {
     // ================================================================ softmax / epilogue ========
+    // Head h = 16 * quad + (lane % 16); lanes l and l + 16 share it, each owning 32 of the
+    // tile's 64 columns (TMEM 16x32bx2 load), so the running max is agreed by one shuffle.
     const int quad = warp & 3;
-    const int h = quad * 16 + lane;           // head row owned by lanes 0..15
-    const bool head_thread = lane < 16;
+    const int hl = lane & 15, half = lane >> 4;
+    const int h = quad * 16 + hl;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    float m_ref = -INFINITY, l_sum = 0.f;
+    {
+      // Q's latent dims (blocks 0-7) bf16 -> fp16 in place; the RoPE block stays bf16
+      const bool qok = warp_wait(q_full, 0, p.err, lane);
+      bool in_range = true;
+      if (qok) {
+        uint4* q4 = reinterpret_cast<uint4*>(sQ);
+        const int sm_tid = tid - (kThreads - kSmThreads);
+        for (int c = sm_tid; c < 8 * kBlk / 16; c += kSmThreads) {
+          uint4 v = q4[c];
+          uint32_t* w = &v.x;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float lo = __uint_as_float(w[u] << 16), hi = __uint_as_float(w[u] & 0xFFFF0000u);
+            in_range &= fabsf(lo) < kF16Max && fabsf(hi) < kF16Max;
+            const __half2 h2 = __floats2half2_rn(lo, hi);
+            w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          q4[c] = v;
+        }
+      }
+      if (!in_range) flag_error(p.err, HS_FLAG_RANGE);
+      if (!qok) *abort_flag = 1;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+    float m_ref = -INFINITY, l_part = 0.f;
     bool ok = true;
 #pragma unroll 1
     for (int i = 0; i < ntiles; ++i) {
@@ -270,9 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t xr[64];
-      tmem_ld32(tmem + lane_base + kColS + 64 * s, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
-      tmem_ld32(tmem + lane_base + kColS + 64 * s + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
+      uint32_t xr[32];
+      tmem_ld16x2_32(tmem + lane_base + kColS + 64 * s, xr);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -280,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // logits in log2 units, in place (as float bits); masked rows become -inf
       float mt = -INFINITY;
       {
-        const uint4* vld4 = reinterpret_cast<const uint4*>(sValid + s * kRows);
+        const uint4* vld4 = reinterpret_cast<const uint4*>(sValid + s * kRows + 32 * half);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 2; ++q4) {
           const uint4 vv = vld4[q4];
           const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
@@ -295,41 +387,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!head_thread) mt = -INFINITY;
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
       const bool need = mt > m_ref + kRescaleThreshold;
       const float m_new = need ? mt : m_ref;
-      w = i == 0 || warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane);
-      if (named_bar_or(1, kSmThreads, !w)) {
-        ok = false;
-        *abort_flag = 1;
-        break;
-      }
       const bool any = named_bar_or(1, kSmThreads, need && i > 0);
-      const float alpha = need ? exp2f(m_ref - m_new) : 1.f;
-      l_sum *= alpha;
+      // P and O^T of the previous tile must be consumed before they are overwritten / rescaled
+      if (i > 0 && !warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane)) *abort_flag = 1;
+      const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;
+      l_part *= alpha;
       m_ref = m_new;
-      if (head_thread) {
+      {
         float psum = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
           uint32_t pk[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int c = ch * 8 + 2 * u;
             const float x0 = __uint_as_float(xr[c]), x1 = __uint_as_float(xr[c + 1]);
-            const float p0 = x0 == -INFINITY ? 0.f : exp2f(x0 - m_ref);
-            const float p1 = x1 == -INFINITY ? 0.f : exp2f(x1 - m_ref);
+            const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m_ref);
+            const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m_ref);
             psum += p0 + p1;
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            pk[u] = *reinterpret_cast<uint32_t*>(&b2);
+            const __half2 h2 = __floats2half2_rn(p0, p1);
+            pk[u] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(sP + sw128_offset(h, ch * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4*>(sP + sw128_offset(h, (4 * half + ch) * 16)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        l_sum += psum;
+        l_part += psum;
       }
       // rescale O^T columns of the heads whose reference max moved (after P: fewer live registers)
       if (any) {
-        if (head_thread) sAlpha[h] = alpha;
+        if (half == 0) sAlpha[h] = alpha;
         named_bar(1, kSmThreads);
         tc_fence_after();
 #pragma unroll 1
@@ -359,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc_fence_after();
-    if (head_thread) {
+    const float l_sum = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+    if (half == 0) {
       sInvL[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
       if (p.lse && h < p.H)
         p.lse[(int64_t)t * p.H + h] = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;

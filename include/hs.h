@@ -69,6 +69,7 @@ typedef enum {
 #define HS_FLAG_NOT_ASCENDING  0x08  /* resolve: a request's indices are not strictly ascending */
 #define HS_FLAG_BAD_STATE      0x10  /* resolve: inconsistent LRU state (slot/token maps disagree) */
 #define HS_FLAG_TIMEOUT        0x20  /* a bounded in-kernel wait ran out */
+#define HS_FLAG_RANGE          0x40  /* sparse MLA: a value outside the 16-bit compute range (see below) */
 
 #define HS_PAGE 64               /* tokens per KV page */
 #define HS_KV_ROW_BYTES 656      /* latent-KV row size */
@@ -165,9 +166,15 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  *   out[t,h,:] = sum_i softmax(logit)_i * latent_i[:]          (bf16, fp32 accumulation)
  *   lse[t,h]   = ln sum_i exp(logit_i)                          (natural log; -inf if no row)
  *
+ * Compute precision: the latent part of q and the dequantised latent rows enter the tensor cores as
+ * IEEE half (fp16, 10-bit mantissa), the RoPE part as bf16, P as fp16, all accumulated in fp32.
+ * fp16 bounds the inputs: |q| < 65504 on the latent dims and group scales in [2^-14, 146]
+ * (so |code * scale| < 65504). A value outside these bounds sets HS_FLAG_RANGE; the result is then
+ * not reliable.
+ *
  * idx entries < 0 are padding and skipped. With block_table == NULL they are physical pool rows
  * (< R); otherwise logical token indices of request token_req[t] mapped through the paged layout.
- * A query with no valid entry gets out = 0 and lse = -inf. Duplicated entries count once each.
+ * A query with no valid entry gets out = 0 and lse = -inf. Each occurrence of a duplicated entry counts.
  *
  *   T, H          query tokens; heads, 1 <= H <= 64
  *   k             entries per idx row

@@ -19,7 +19,7 @@ def _rows(n, seed, group_scales=False):
     rope = st.sub("r").normal((n, 64))
     gs = None
     if group_scales:
-        gs = (np.abs(lat).reshape(n, 4, 128).max(-1) / 448 * np.array([1.0, 3.0, 1.5, 7.0])).astype(np.float32)
+        gs = (np.abs(lat).reshape(n, 4, 128).max(-1) / 448 * np.array([1.25, 3.0, 1.5, 7.0])).astype(np.float32)
     return inputs.pack_kv_rows(lat, rope, gs)
 
 
@@ -60,7 +60,7 @@ def test_random_index_sets(H, k, n):
 def test_distinct_group_scales_and_large_logits():
     n, T, H, k = 600, 5, 64, 512
     kv = _rows(n, seed=3, group_scales=True)
-    q = inputs.bf16_bits(inputs.Stream(4).sub("q").normal((T, H, 576), sigma=3.0))  # peaky softmax
+    q = inputs.bf16_bits(inputs.Stream(4).sub("q").normal((T, H, 576), sigma=1.5))  # peaky softmax (logit std ~4.5)
     rng = np.random.default_rng(0)
     idx = np.stack([rng.permutation(n)[:k] for _ in range(T)]).astype(np.int32)
     out, lse, flag = _run(q, kv, idx, 0.125)
@@ -101,3 +101,17 @@ def test_host_side_validation():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(HSError):
         hs_sparse_mla_fwd(q, kv, idx, 1.0, out, err)   # H = 65 > 64
+
+
+def test_out_of_fp16_range_scale_is_flagged():
+    """A group scale too large for the fp16 compute path sets HS_FLAG_RANGE (0x40)."""
+    n = 64
+    lat = np.zeros((n, 512), np.float32)
+    gs = np.full((n, 4), 0.01, np.float32)
+    gs[7, 2] = 1000.0
+    kv = inputs.pack_kv_rows(lat, np.zeros((n, 64), np.float32), gs)
+    q = inputs.bf16_bits(np.ones((1, 4, 576), np.float32))
+    _, _, flag = _run(q, kv, np.arange(n, dtype=np.int32)[None], 0.05)
+    assert flag & 0x40
+    _, _, flag = _run(q, kv, np.array([[0, 1, 2, 3]], np.int32), 0.05)
+    assert flag == 0
