@@ -335,7 +335,7 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         import oracle
         threads = oracle.num_threads(0)
-        sample = list(range(min(w.T, max(4, threads))))
+        sample = list(range(min(w.T, max(16, 4 * threads))))  # ~10-30 s of CPU work
         wall_cpu = oracle_sample(w, sample, threads=0)
         cpu = {"value": round(len(sample) / wall_cpu, 3), "unit": "tokens/s", "cores": min(threads, len(sample)),
                "kind": "oracle", "sample": "%d query tokens of the same batch (first %d requests), full "
