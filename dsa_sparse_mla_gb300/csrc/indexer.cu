@@ -14,7 +14,9 @@
 //
 // Roles (320 threads): warp 0 issues TMA loads (query tile once, two 64-key pages per stage),
 // warp 1 allocates TMEM and issues tcgen05.mma (e4m3 x e4m3 -> fp32, M=128, N=256, K=32),
-// warps 2..9 drain the two TMEM accumulators (each warp: its 32-lane quarter, half the columns).
+// warps 2..9 drain the two TMEM accumulators: each warp owns its 32-lane quarter and a 128-column
+// slice, reads the slice into registers, hands the accumulator back to the MMA at once, and only then
+// does the arithmetic (so the tensor pipe never waits for the ALU work of the tile before).
 #include "common.cuh"
 
 namespace hs {
@@ -23,7 +25,8 @@ namespace indexer {
 constexpr int kBlockM = 128;   // keys per tile (two pages)
 constexpr int kN = 256;        // (token, head) columns per group
 constexpr int kStages = 6;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 8;    // two per TMEM lane quarter; 10 warps leave 168 registers a thread
+constexpr int kSlice = kN * 4 / kEpiWarps;  // accumulator columns per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxG = 32;      // tokens per group when Hi = 8
 constexpr int kMaxTpc = 64;    // tiles per CTA and segment
@@ -42,6 +45,7 @@ struct Params {
   int64_t ld;
   int32_t* err;
   int32_t tiles_per_cta;
+  int32_t scale_prefetch;  // k_scale is 16-byte aligned: pull each page's 64 scales into L2 early
 };
 
 template <int DI, int HI>
@@ -58,7 +62,8 @@ struct Cfg {
   static constexpr int kOffTok = kOffW + kN * 4;              // int32 x 4 x kMaxG
   static constexpr int kOffSeg = kOffTok + 4 * kMaxG * 4;     // int32 x 4 x kMaxG
   static constexpr int kOffBlk = kOffSeg + 4 * kMaxG * 4;   // int32 [kMaxG][2 * kMaxTpc]
-  static constexpr int kOffBar = kOffBlk + kMaxG * 2 * kMaxTpc * 4;
+  static constexpr int kOffLim = kOffBlk + kMaxG * 2 * kMaxTpc * 4;  // int32 [kMaxG][kMaxG]
+  static constexpr int kOffBar = kOffLim + kMaxG * kMaxG * 4;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 64 + 1024;          // + alignment slack
@@ -82,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* sSegLo = sSegN + kMaxG;                       // first tile of this CTA
   int32_t* sSegHi = sSegLo + kMaxG;                      // one past the last tile
   int32_t* sBlk = (int32_t*)(smem + C::kOffBlk);         // physical page of each of the CTA's pages
+  int32_t* sLim = (int32_t*)(smem + C::kOffLim);         // [segment][token]: visible keys, 0 = other request
   uint64_t* bars = (uint64_t*)(smem + C::kOffBar);
   uint64_t* full = bars;                                 // [kStages]
   uint64_t* empty = bars + kStages;                      // [kStages]
@@ -165,6 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = nseg;
   }
   __syncthreads();
+  // keys token g may see while the CTA scores segment s (0 when g belongs to another request)
+  for (int i = tid; i < misc[0] * G; i += kThreads) {
+    const int sg = i / G, g = i % G;
+    sLim[sg * kMaxG + g] = sTokSeg[g] == sg ? sTokN[g] : 0;
+  }
   // stage this CTA's block-table entries (2 pages per tile) so no warp waits on them later
   for (int s = 0; s < misc[0]; ++s) {
     const int r = sSegReq[s];
@@ -214,8 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive_expect_tx(&full[st], bytes);
             for (int pg = 0; pg < 2; ++pg)
-              if (blk[pg] >= 0)
+              if (blk[pg] >= 0) {
                 tma_load_2d(sK + st * C::kTileBytes + pg * 64 * DI, &map_k, &full[st], 0, blk[pg] * 64);
+                if (p.scale_prefetch) bulk_prefetch_l2(p.k_scale + (int64_t)blk[pg] * 64, 64 * 4);
+              }
           }
         }
         // every issued copy must land before the CTA's shared memory is released
@@ -259,72 +272,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ------------------------------------------------------------ epilogue --------------------
+      constexpr int kTok = kSlice / HI;  // tokens in a warp's column slice
       const int quad = warp & 3;
-      const int half = (warp - 2) >> 2;  // which half of the 256 columns
-      const int row = quad * 32 + lane;
-      // key scale of this thread's key in item (s, kt); < 0 marks a key outside the request
-      auto key_scale = [&](int s, int kt) -> float {
-        const int64_t j = (int64_t)kt * kBlockM + row;
-        if (j >= sSegN[s]) return -1.f;
-        const int32_t blk = sBlk[s * 2 * kMaxTpc + 2 * (kt - sSegLo[s]) + (row >> 6)];
-        return blk >= 0 ? __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63)) : -1.f;
-      };
-      int s = 0;
-      while (s < nseg && sSegHi[s] <= sSegLo[s]) ++s;
-      int kt = s < nseg ? sSegLo[s] : 0;
-      float ks = s < nseg ? key_scale(s, kt) : -1.f;
-      for (int it = 0; it < total; ++it) {
-        // next item, and its key scale fetched before waiting (its latency overlaps this tile)
-        int s2 = s, kt2 = kt + 1;
-        while (s2 < nseg && kt2 >= sSegHi[s2]) {
-          ++s2;
-          kt2 = s2 < nseg ? sSegLo[s2] : 0;
-        }
-        const float ks2 = s2 < nseg ? key_scale(s2, kt2) : -1.f;
-        const int b = it & 1;
-        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-        const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
-        if (!__all_sync(0xffffffffu, go)) {
-          *abort_flag = 1;
-          break;
-        }
-        tc_fence_after();
-        const int64_t j = (int64_t)kt * kBlockM + row;
-        const bool key_ok = ks >= 0.f;
-#pragma unroll 1
-        for (int gi = 0; gi < G / 2; ++gi) {
-          const int g = half * (G / 2) + gi;
-          if (sTokSeg[g] != s) continue;  // warp-uniform
-          uint32_t acc[HI];
-          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kN + g * HI);
-          if constexpr (HI >= 32) {
-#pragma unroll
-            for (int c = 0; c < HI; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<uint32_t(*)[32]>(&acc[c]));
-          } else {
-#pragma unroll
-            for (int c = 0; c < HI; c += 8) tmem_ld8(taddr + c, *reinterpret_cast<uint32_t(*)[8]>(&acc[c]));
+      const int slice = (warp - 2) >> 2;
+      const int row = quad * 32 + lane;  // key of the tile (TMEM lane)
+      const int g0 = slice * kTok;       // first token of the slice (group-local)
+      static_assert(kSlice % HI == 0 && kSlice % 32 == 0, "slice holds whole tokens");
+      const float* wsl = sW + slice * kSlice;
+      float* const srow = p.scores + (int64_t)(t0 + g0) * p.ld + row;  // used only where lim > 0
+      int it = 0;
+      bool ok = true;
+      for (int s = 0; s < nseg && ok; ++s) {
+        const int lo = sSegLo[s], hi = sSegHi[s];
+        const int jn = sSegN[s];                                    // keys of the segment's longest token
+        const int32_t* blk_s = sBlk + s * 2 * kMaxTpc - 2 * lo;     // page of (tile kt, half) at 2 kt + half
+        const int32_t* lim_s = sLim + s * kMaxG + g0;
+        // key scale of this thread's key in tile kt; < 0 marks a key outside the request
+        auto key_scale = [&](int kt) -> float {
+          const int j = kt * kBlockM + row;
+          if (j >= jn) return -1.f;
+          const int32_t blk = blk_s[2 * kt + (row >> 6)];
+          return blk >= 0 ? __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63)) : -1.f;
+        };
+        float ks = lo < hi ? key_scale(lo) : -1.f;
+        for (int kt = lo; kt < hi; ++kt, ++it) {
+          // next tile's key scale, fetched before waiting (its latency overlaps this tile; the
+          // producer has already pulled the scales into L2 together with the keys)
+          const float ks_next = kt + 1 < hi ? key_scale(kt + 1) : -1.f;
+          const int b = it & 1;
+          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+          const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
+          if (!__all_sync(0xffffffffu, go)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kN + slice * kSlice);
+          uint32_t acc[kSlice / 32][32];
+#pragma unroll
+          for (int q = 0; q < kSlice / 32; ++q) tmem_ld32(taddr + 32 * q, acc[q]);
           tmem_wait_ld();
-          // sum_h w'[h] * relu(dot[h]): half the ReLUs on the ALU pipe (max), half on the FMA
-          // pipe (x + |x|), products accumulated with packed fp32x2 FMAs
-          const float* w = sW + g * HI;
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          // the slice is in registers: the accumulator may take the next MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+          const int j = kt * kBlockM + row;
 #pragma unroll
-          for (int h = 0; h < HI; h += 4) {
-            const float4 wv = *reinterpret_cast<const float4*>(w + h);
-            const float x0 = __uint_as_float(acc[h]), x1 = __uint_as_float(acc[h + 1]);
-            const float x2 = __uint_as_float(acc[h + 2]), x3 = __uint_as_float(acc[h + 3]);
-            ffma2(s0, s1, fmaxf(x0, 0.f), fmaxf(x1, 0.f), wv.x, wv.y);
-            ffma2(s2, s3, x2 + fabsf(x2), x3 + fabsf(x3), wv.z, wv.w);
+          for (int k = 0; k < kTok; ++k) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int h = 0; h < HI; h += 4) {
+              const int c = k * HI + h;
+              const float4 wv = *reinterpret_cast<const float4*>(wsl + c);
+              const float x0 = __uint_as_float(acc[c / 32][c % 32]);
+              const float x1 = __uint_as_float(acc[c / 32][c % 32 + 1]);
+              const float x2 = __uint_as_float(acc[c / 32][c % 32 + 2]);
+              const float x3 = __uint_as_float(acc[c / 32][c % 32 + 3]);
+              ffma2(a0, a1, fmaxf(x0, 0.f), fmaxf(x1, 0.f), wv.x, wv.y);
+              ffma2(a2, a3, x2 + fabsf(x2), x3 + fabsf(x3), wv.z, wv.w);
+            }
+            if (ks >= 0.f && j < lim_s[k])
+              srow[(int64_t)k * p.ld + (int64_t)kt * kBlockM] = ks * ((a0 + a1) + (a2 + a3));
           }
-          if (key_ok && j < sTokN[g]) p.scores[(int64_t)(t0 + g) * p.ld + j] = ks * ((s0 + s1) + (s2 + s3));
+          ks = ks_next;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
-        s = s2;
-        kt = kt2;
-        ks = ks2;
       }
     }
   }
@@ -388,6 +400,7 @@ cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t s
   if (tpc < 8) tpc = 8;
   if (tpc > 64) tpc = 64;
   p.tiles_per_cta = (int)tpc;
+  p.scale_prefetch = ((uintptr_t)a->k_scale & 15) == 0 ? 1 : 0;
   int splits = (int)((tiles_max + tpc - 1) / tpc);
   if (splits < 1) splits = 1;
   if (groups == 0) return cudaSuccess;
