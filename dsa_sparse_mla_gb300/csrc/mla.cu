@@ -6,11 +6,15 @@
 // dims. Per query token t, head h, over the valid entries i of idx[t, :]:
 //   logit_i = scale * <q[t,h,:], [latent_i, rope_i]>,  out = softmax(logit) . latent,  lse = ln sum exp.
 //
-// One CTA per query token (416 threads):
-//   warps 0-7   gather 64 rows per tile (a warp per row at a time, 16-byte coalesced loads),
-//               dequantise latent = e4m3 * group scale to fp16 (exact e4m3 -> fp16 conversion, one
-//               rounding for the scale) and write it, with the bf16 RoPE part as stored, into a
-//               128-byte-swizzled [dim block][row] tile (2 stages);
+// One CTA per query token (448 threads):
+//   warps 0-7   gather 64 rows per tile (warp w owns rows 8w..8w+7; one 16-byte load per lane
+//               brings one 64-dim block of all 8 rows), dequantise latent = e4m3 * group scale to
+//               fp16 (exact e4m3 -> fp16 conversion, one rounding for the scale) and write it, with
+//               the bf16 RoPE part as stored, into a 128-byte-swizzled [dim block][row] tile
+//               (2 stages). Blocks are published in pairs as soon as they are written (a barrier
+//               per block), so QK starts on the first blocks while later ones are still being
+//               written; PV releases the stage pair by pair (one barrier per 128-dim M-tile),
+//               so the next tile's first blocks are written while PV still reads the last ones;
 //   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 64 rows,
 //               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile and an S
 //               buffer are ready;
@@ -20,8 +24,9 @@
 //               dequantised once. Producers load and dequantise the next tile into registers
 //               while they wait for a free stage, so global-memory latency is off the MMA chain;
 //   warps 10-13 first convert Q's latent dims to fp16 in shared memory, then run the online
-//               softmax: two threads share each head's row of S (one shuffle for the max); P goes to
-//               shared memory as fp16. O^T lives in TMEM and is rescaled only
+//               softmax: two threads share each head's row of S (one shuffle for the max); P goes
+//               as fp16 into the stage's RoPE block, which QK no longer needs, so P is double
+//               buffered with the stages. O^T lives in TMEM and is rescaled only
 //               when a head's running max grows by more than 2^8 (lazy rescaling); the final pass
 //               divides by the row sum and writes bf16.
 // TMEM: columns 0-127 hold two S buffers (64-row layout), 128-383 hold O^T.
@@ -41,15 +46,16 @@ constexpr uint32_t kColO = 128;
 constexpr int kBlk = 8192;                 // one [64 rows][128 B] swizzled block
 constexpr int kQBytes = 9 * kBlk;          // 64 heads x 576 bf16
 constexpr int kStageBytes = 9 * kBlk;      // 64 rows x (512 latent + 64 rope) bf16
-constexpr int kPBytes = kBlk;              // 64 heads x 64 rows bf16
+constexpr int kBlocks = 9;                 // 8 latent dim blocks + the RoPE block (later P)
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kQBytes;
-constexpr int kOffP = kOffStage + 2 * kStageBytes;
-constexpr int kOffValid = kOffP + kPBytes;          // uint8 [2][64]
+constexpr int kOffValid = kOffStage + 2 * kStageBytes;  // uint8 [2][64]
 constexpr int kOffAlpha = kOffValid + 128;          // float [64]
 constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
-constexpr int kOffBar = kOffInvL + 256;             // 14 barriers
-constexpr int kOffMisc = kOffBar + 14 * 8;          // tmem base, abort
+constexpr int kEmpty = 5;                 // per stage: 4 latent block pairs (one PV M-tile each) + RoPE/P
+constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 10;
+constexpr int kOffBar = kOffInvL + 256;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort
 constexpr int kSmem = kOffMisc + 16 + 1024;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
@@ -91,21 +97,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sStage = smem + kOffStage;
-  uint8_t* sP = smem + kOffP;
   uint8_t* sValid = smem + kOffValid;
   float* sAlpha = (float*)(smem + kOffAlpha);
   float* sInvL = (float*)(smem + kOffInvL);
   uint64_t* bars = (uint64_t*)(smem + kOffBar);
-  uint64_t* full = bars + 0;      // [2] producers -> MMA, softmax
-  uint64_t* empty = bars + 2;     // [2] PV done with the stage -> producers
-  uint64_t* s_full = bars + 4;    // [2] QK done -> softmax
-  uint64_t* s_free = bars + 6;    // [2] softmax read S -> MMA
-  uint64_t* p_ready = bars + 8;   // softmax wrote P (and corrected O) -> MMA
-  uint64_t* pv_done = bars + 9;   // PV done -> softmax
-  uint64_t* q_full = bars + 10;
-  uint64_t* mma_done = bars + 11;  // QK issuer's MMAs drained
-  uint64_t* pv_drain = bars + 12;  // PV issuer's MMAs drained
-  uint64_t* q_ready = bars + 13;   // Q converted to fp16 (latent dims) -> QK issuer
+  uint64_t* full = bars + 0;                 // [2][9] producers wrote dim block b -> QK
+  uint64_t* empty = bars + 2 * kBlocks;      // [2][5] PV done with block pair m (m = 4: RoPE/P) -> producers
+  uint64_t* s_full = empty + 2 * kEmpty;     // [2] QK done -> softmax
+  uint64_t* s_free = s_full + 2;             // [2] softmax read S -> MMA
+  uint64_t* p_ready = s_full + 4;            // softmax wrote P (and corrected O) -> MMA
+  uint64_t* pv_done = s_full + 5;            // PV done -> softmax
+  uint64_t* q_full = s_full + 6;
+  uint64_t* mma_done = s_full + 7;           // QK issuer's MMAs drained
+  uint64_t* pv_drain = s_full + 8;           // PV issuer's MMAs drained
+  uint64_t* q_ready = s_full + 9;            // Q converted to fp16 (latent dims) -> QK issuer
   uint32_t* misc = (uint32_t*)(smem + kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 
@@ -115,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (k + kRows - 1) / kRows;
 
   if (tid == 0) {
+    for (int i = 0; i < 2 * kBlocks; ++i) mbar_init(&full[i], kProdWarps);
+    for (int i = 0; i < 2 * kEmpty; ++i) mbar_init(&empty[i], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&full[i], kProdWarps);
-      mbar_init(&empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
     }
@@ -137,16 +142,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProdWarps) {
     // ================================================================ gather + dequantise ======
-    // Warp w owns rows 8w .. 8w+7 of every tile. For one row, lane j loads latent bytes
-    // [16j, 16j+16) (the whole 512-byte latent in one coalesced instruction), lanes 0-3 the four
-    // group scales and lanes 4-11 the 128-byte RoPE part. Software pipeline per warp:
+    // Warp w owns rows 8w .. 8w+7 of every tile. Lane l works on row 8w + (l >> 2): for dim block
+    // b (64 latent dims) it loads bytes [64b + 16(l & 3), +16) of that row, so one instruction
+    // brings block b of all 8 rows. The RoPE part (128 bytes a row) takes two instructions
+    // (lane l: row 8w + 4h + (l >> 3), bytes 16(l & 7)..), the group scales one (lanes 0-7).
+    // Software pipeline per warp:
     //   tile i+4: index entries (lanes 0-7)     tile i+3: block-table entries
     //   tile i+2: rows prefetched into L2 by the TMA engine (one 656-byte bulk prefetch per row)
     //   tile i+1: row data loaded into registers
-    //   tile i  : dequantised into its stage once the stage is free.
+    //   tile i  : dequantised into its stage, block by block, once the stage is free.
     // Loads are volatile so they are issued here and not next to their first use.
     const int req = p.bt ? p.token_req[t] : 0;
     const int64_t idx_base = (int64_t)t * k;
+    const int sub = lane & 3;          // 16-byte piece of a 64-byte latent block
+    const int rlat = lane >> 2;        // row (within the warp's 8) of the latent pieces
+    const int rrope = lane >> 3;       // row (within a 4-row half) of the RoPE pieces
     auto ld_idx = [&](int i) -> int32_t {  // lane rr < 8: index entry of row 8 * warp + rr of tile i
       const int e = i * kRows + warp * 8 + lane;
       return (lane < 8 && i < ntiles && e < k) ? ldg_nc_s32(p.idx + idx_base + e) : -1;
@@ -165,58 +175,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return r;
     };
-    uint4 lat[8], rope[8];     // row data of the next tile: latent (all lanes), RoPE (lanes 4-11)
-    float scl[8];              // lanes 0-3: group scale (lane) of each row
+    uint4 lat[8];              // next tile: latent block b of row rlat (16 codes)
+    uint4 rope[2];             // next tile: RoPE half h, row 4h + rrope (8 bf16)
+    float4 scl = make_float4(0.f, 0.f, 0.f, 0.f);  // lanes 0-7: group scales of row lane
     int64_t my_row = -1;       // lanes 0-7: physical row of the tile whose data is loaded
     auto ld_rows = [&](int64_t rows_lane) {
+      const int64_t r0 = __shfl_sync(0xffffffffu, rows_lane, rlat);
+      const int64_t r1 = __shfl_sync(0xffffffffu, rows_lane, rrope);
+      const int64_t r2 = __shfl_sync(0xffffffffu, rows_lane, 4 + rrope);
+      const uint8_t* src = p.kv + (r0 >= 0 ? r0 : 0) * HS_KV_ROW_BYTES + 16 * sub;
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int64_t r = __shfl_sync(0xffffffffu, rows_lane, rr);
-        lat[rr] = make_uint4(0, 0, 0, 0);
-        rope[rr] = make_uint4(0, 0, 0, 0);
-        scl[rr] = 0.f;
-        if (r >= 0) {
-          const uint8_t* src = p.kv + r * HS_KV_ROW_BYTES;
-          lat[rr] = ldg_nc_v4(src + 16 * lane);
-          if (lane < 4) scl[rr] = ldg_nc_f32(src + HS_D_LATENT + 4 * lane);
-          else if (lane < 12) rope[rr] = ldg_nc_v4(src + HS_D_LATENT + 16 + 16 * (lane - 4));
-        }
+      for (int b = 0; b < 8; ++b) lat[b] = r0 >= 0 ? ldg_nc_v4(src + 64 * b) : make_uint4(0, 0, 0, 0);
+      rope[0] = r1 >= 0 ? ldg_nc_v4(p.kv + r1 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
+                        : make_uint4(0, 0, 0, 0);
+      rope[1] = r2 >= 0 ? ldg_nc_v4(p.kv + r2 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
+                        : make_uint4(0, 0, 0, 0);
+      if (lane < 8 && rows_lane >= 0) {
+        const uint4 v = ldg_nc_v4(p.kv + rows_lane * HS_KV_ROW_BYTES + HS_D_LATENT);
+        scl = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+      } else {
+        scl = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     };
-    // waits for stage i % 2, dequantises the loaded rows into it and publishes it; false on abort
+    // dequantises the loaded rows into stage i % 2 block by block: each block pair is written as
+    // soon as PV of the tile that used the stage before has released it, and published at once;
+    // false on abort
+    auto wait_empty = [&](int s, int m, int i) -> bool {
+      int go = 1;
+      if (lane == 0) go = !*abort_flag && mbar_wait(&empty[s * kEmpty + m], ((uint32_t)(i >> 1) & 1u) ^ 1u, p.err);
+      go = __shfl_sync(0xffffffffu, go, 0);
+      if (!go && lane == 0) *abort_flag = 1;
+      return go != 0;
+    };
     auto publish = [&](int i) -> bool {
       const int s = i & 1;
-      int go = 1;
-      if (lane == 0) go = !*abort_flag && mbar_wait(&empty[s], ((uint32_t)(i >> 1) & 1u) ^ 1u, p.err);
-      if (!__shfl_sync(0xffffffffu, go, 0)) {
-        if (lane == 0) *abort_flag = 1;
-        return false;
-      }
+      if (!wait_empty(s, 0, i)) return false;
       uint8_t* st = sStage + s * kStageBytes;
-      uint8_t* blk = st + (lane >> 2) * kBlk;  // dim block of dims 16 * lane .. +15
-      const int ch0 = (lane & 3) * 2;
-      const int first = (lane >> 2) & 1;    // store order alternates so a store hits 8 bank groups
+      uint64_t* fb = full + s * kBlocks;
+      if (lane < 8) sValid[s * kRows + warp * 8 + lane] = my_row >= 0 ? 1 : 0;
+      const int row = warp * 8 + rlat;
       bool range_ok = true;
 #pragma unroll
-      for (int rr = 0; rr < 8; ++rr) {
-        const int row = warp * 8 + rr;
-        const float scale = __shfl_sync(0xffffffffu, scl[rr], lane >> 3);
+      for (int g = 0; g < 4; ++g) {
+        if (g > 0 && !wait_empty(s, g, i)) return false;
+        const float sg = g == 0 ? scl.x : g == 1 ? scl.y : g == 2 ? scl.z : scl.w;
+        const float scale = __shfl_sync(0xffffffffu, sg, rlat);
         range_ok &= scale == 0.f || (fabsf(scale) >= kScaleMin && fabsf(scale) <= kScaleMax);
         const __half2 s2 = __float2half2_rn(scale);
         const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
-        const uint4 v = lat[rr];
-        const uint4 lo = dequant8_f16(v.x, v.y, s2u);
-        const uint4 hi = dequant8_f16(v.z, v.w, s2u);
-        *reinterpret_cast<uint4*>(blk + sw128_offset(row, (ch0 + first) * 16)) = first ? hi : lo;
-        *reinterpret_cast<uint4*>(blk + sw128_offset(row, (ch0 + 1 - first) * 16)) = first ? lo : hi;
-        if (lane >= 4 && lane < 12)  // RoPE piece lane-4 -> dim block 8, kept in bf16
-          *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(row, (lane - 4) * 16)) = rope[rr];
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = 2 * g + bb;
+          const uint4 v = lat[b];
+          const uint4 lo = dequant8_f16(v.x, v.y, s2u);
+          const uint4 hi = dequant8_f16(v.z, v.w, s2u);
+          uint8_t* blk = st + b * kBlk;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * sub)) = lo;
+          *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * sub + 16)) = hi;
+        }
+        // publish the pair (one proxy fence per pair: each fence + arrive costs ~50 cycles)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&fb[2 * g]);
+          mbar_arrive(&fb[2 * g + 1]);
+        }
       }
+      // RoPE block (bf16 as stored); it held P of the tile before, released last
+      if (!wait_empty(s, 4, i)) return false;
+      *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(warp * 8 + rrope, 16 * (lane & 7))) = rope[0];
+      *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(warp * 8 + 4 + rrope, 16 * (lane & 7))) = rope[1];
       if (!range_ok) flag_error(p.err, HS_FLAG_RANGE);
-      if (lane < 8) sValid[s * kRows + warp * 8 + lane] = my_row >= 0 ? 1 : 0;
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&full[s]);
+      if (lane == 0) mbar_arrive(&fb[8]);
       return true;
     };
     // prologue: tile 0 in registers, tile 1 prefetched into L2, tile 2 block entries and tile 3
@@ -262,15 +294,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < ntiles && ok; ++i) {
         const int s = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-        if (*abort_flag || !mbar_wait(&full[s], ph, p.err) || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
+        if (*abort_flag || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
           ok = false;
           break;
         }
-        tc_fence_after();
         const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
         const uint32_t d = tmem + kColS + 64 * s;
 #pragma unroll
-        for (int db = 0; db < 9; ++db) {
+        for (int db = 0; db < kBlocks; ++db) {
+          // dim block db of this tile written by all producer warps
+          if (!mbar_wait(&full[s * kBlocks + db], ph, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t a = smem_desc(q_addr + db * kBlk + kk * 32, 16, 1024, 2);
@@ -278,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16_ss(d, a, b, db < 8 ? idesc_qk : idesc_qk_rope, (db | kk) != 0 ? 1u : 0u);
           }
         }
+        if (!ok) break;
         mma_commit(&s_full[s]);
       }
       if (!ok) *abort_flag = 1;
@@ -289,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ PV issuer =================
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
-      const uint32_t st_addr = smem_u32(sStage), p_addr = smem_u32(sP);
+      const uint32_t st_addr = smem_u32(sStage);
       bool ok = true;
 #pragma unroll 1
       for (int j = 0; j < ntiles; ++j) {
@@ -299,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t sa = st_addr + (uint32_t)((j & 1) * kStageBytes);
+        const uint32_t p_addr = sa + 8 * kBlk;  // P of this tile in the stage's RoPE block
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -307,9 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t b = smem_desc(p_addr + kk * 32, 16, 1024, 2);
             mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
+          mma_commit(&empty[(j & 1) * kEmpty + mt]);  // dim blocks 2mt, 2mt+1 may be refilled
         }
         mma_commit(pv_done);
-        mma_commit(&empty[j & 1]);
+        mma_commit(&empty[(j & 1) * kEmpty + 4]);     // P (the RoPE block) consumed
       }
       if (!ok) *abort_flag = 1;
       mma_commit(pv_drain);
@@ -356,7 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i & 1;
       const uint32_t ph = (uint32_t)(i >> 1) & 1u;
       // every exit decision is taken by all four softmax warps together (no partial barriers)
-      bool w = !*abort_flag && warp_wait(&s_full[s], ph, p.err, lane) && warp_wait(&full[s], ph, p.err, lane);
+      // (the last block barrier also orders the producers' row-validity bytes before the reads below)
+      bool w = !*abort_flag && warp_wait(&s_full[s], ph, p.err, lane) &&
+               warp_wait(&full[s * kBlocks + kBlocks - 1], ph, p.err, lane);
       if (named_bar_or(1, kSmThreads, !w)) {
         ok = false;
         *abort_flag = 1;
@@ -391,12 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need = mt > m_ref + kRescaleThreshold;
       const float m_new = need ? mt : m_ref;
       const bool any = named_bar_or(1, kSmThreads, need && i > 0);
-      // P and O^T of the previous tile must be consumed before they are overwritten / rescaled
-      if (i > 0 && !warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane)) *abort_flag = 1;
       const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;
       l_part *= alpha;
       m_ref = m_new;
       {
+        // P goes into this stage's RoPE block: QK of the tile has finished reading it (s_full), and
+        // the stage is not rewritten before PV of the tile releases it
+        uint8_t* sPt = sStage + s * kStageBytes + 8 * kBlk;
         float psum = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
@@ -411,11 +454,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __half2 h2 = __floats2half2_rn(p0, p1);
             pk[u] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(sP + sw128_offset(h, (4 * half + ch) * 16)) =
+          *reinterpret_cast<uint4*>(sPt + sw128_offset(h, (4 * half + ch) * 16)) =
               make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         l_part += psum;
       }
+      // PV of the previous tile must have finished accumulating into O^T before it is rescaled and
+      // before this tile's PV is released. Waiting on every tile (after P is written: P is double
+      // buffered with the stages, so this costs no overlap) keeps this warp at most one phase
+      // behind the barrier, which its parity-based wait requires.
+      if (i > 0 && !warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane)) *abort_flag = 1;
       // rescale O^T columns of the heads whose reference max moved (after P: fewer live registers)
       if (any) {
         if (half == 0) sAlpha[h] = alpha;
