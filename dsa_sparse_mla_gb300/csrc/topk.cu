@@ -8,7 +8,23 @@
 // One CTA of 512 threads per query (two CTAs share an SM). Each score maps to an unsigned key whose
 // order is the score order (sign flip trick), so selection is exact integer work. Each warp owns a
 // contiguous chunk of the row and streams it with the next step's loads issued before the current
-// step is processed (every pass is a walk over L2-resident data, so latency, not bandwidth, rules).
+// step is processed.
+//
+// Fast path (one full pass over the row):
+//   sample: about 1/16 of the row (evenly spaced 128-score blocks) gives a key threshold tau that
+//           roughly 1.5 k scores of the row reach (adaptive histogram of the sample);
+//   filter: one pass appends the index of every score whose key is >= tau to its warp's region
+//           of a shared candidate list (ballots give the positions; keys are re-read later);
+//   select: an adaptive histogram of the candidates finds the bin holding the k-th largest; the
+//           few candidates in it are sorted by (key descending, index ascending), which fixes the
+//           exact composite threshold T; every candidate at or above T is kept;
+//   write:  kept indices are marked in a shared bitmap of the row, and a block-wide prefix sum of
+//           the bitmap's popcounts writes them in ascending order.
+// The fast path gives up (and the exact path below runs) when the row has more than 262,144
+// scores, when the filter finds fewer than k candidates or more than 512 in one warp's chunk, or
+// when more than 1,024 candidates share the threshold bin.
+//
+// Exact path (several passes, any data):
 //   pass 0: min and max key of the row;
 //   pass 1: histograms of (key - lo) >> shift over 8192 bins, shift chosen so the live key range
 //           [lo, hi] fills the bins, narrow [lo, hi] until its keys fit the candidate buffer.
@@ -28,7 +44,15 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 8192;
 constexpr int kMaxCand = 4096;
-constexpr int kSmem = kBins * 4 + kMaxCand * 8;
+constexpr int kSelBins = 4096;         // fast path: sample and candidate histograms
+constexpr int kFastCand = kMaxCand * 2;  // fast path: candidate indices (uint32, same memory as cand)
+constexpr int kSample = 4096;          // fast path: sampled scores (at most)
+constexpr int kSmallSort = 1024;       // fast path: candidates of the threshold bin (at most)
+constexpr int kBitmapWords = 8192;     // fast path: rows of up to 262,144 scores
+constexpr int kOffCand = 0;                            // uint64 [kMaxCand] (sample keys alias it)
+constexpr int kOffHist = kOffCand + kMaxCand * 8;      // uint32 [kBins]
+constexpr int kOffBitmap = kOffHist + kBins * 4;       // uint32 [kBitmapWords] (+ small sort buffer)
+constexpr int kSmem = kOffBitmap + kBitmapWords * 4;
 
 // Order-preserving key: x + 0 turns -0 into +0; negative numbers flip all bits, others the sign;
 // NaN maps to 0 (below every number).
@@ -74,12 +98,335 @@ __device__ __forceinline__ void walk_chunk(const float* row, int c0, int c1, boo
   }
 }
 
+// As walk_chunk, handing the raw scores instead of keys: f(j0, x[4], valid_mask).
+template <typename F>
+__device__ __forceinline__ void walk_chunk_f(const float* row, int c0, int c1, bool vec, F&& f) {
+  const int lane = threadIdx.x & 31;
+  for (int s0 = c0; s0 < c1; s0 += 128 * kDepth) {
+    float4 v[kDepth];
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) {
+      const int j0 = s0 + 128 * d + 4 * lane;
+      if (vec && j0 + 4 <= c1) {
+        v[d] = __ldg(reinterpret_cast<const float4*>(row + j0));
+      } else {
+        v[d].x = j0 < c1 ? __ldg(row + j0) : 0.f;
+        v[d].y = j0 + 1 < c1 ? __ldg(row + j0 + 1) : 0.f;
+        v[d].z = j0 + 2 < c1 ? __ldg(row + j0 + 2) : 0.f;
+        v[d].w = j0 + 3 < c1 ? __ldg(row + j0 + 3) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) {
+      const int sd = s0 + 128 * d;
+      if (sd >= c1) break;  // warp-uniform
+      const int j0 = sd + 4 * lane;
+      const float x[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+      const uint32_t valid = sd + 128 <= c1 ? 0xFu : (uint32_t)((j0 < c1) | ((j0 + 1 < c1) << 1) |
+                                                                ((j0 + 2 < c1) << 2) | ((j0 + 3 < c1) << 3));
+      f(j0, x, valid);
+    }
+  }
+}
+
+// Block-wide exclusive prefix sum of one value per thread; also returns the total.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* part, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) part[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t x = part[w];
+    before += w < warp ? x : 0u;
+    all += x;
+  }
+  __syncthreads();
+  total = all;
+  return before + incl - v;
+}
+
+// Over bins [0, nb) (nb <= kSelBins), finds the bin where the count accumulated from the top
+// reaches `need`: returns it with the count strictly above it (in *above) and its own count.
+__device__ __forceinline__ uint32_t bin_from_top(const uint32_t* hist, uint32_t nb, uint32_t need, uint32_t* part,
+                                                 uint32_t* sh, uint32_t& above, uint32_t& count) {
+  constexpr int kPerT = kSelBins / kThreads;
+  const int tid = threadIdx.x;
+  uint32_t csum = 0;
+#pragma unroll
+  for (int u = 0; u < kPerT; ++u) {
+    const uint32_t rb = kPerT * tid + u;
+    csum += rb < nb ? hist[nb - 1 - rb] : 0u;
+  }
+  uint32_t total;
+  uint32_t run = block_excl_scan(csum, part, total);
+  if (tid == 0) {
+    sh[0] = 0xFFFFFFFFu;
+    sh[1] = 0;
+    sh[2] = 0;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int u = 0; u < kPerT; ++u) {
+    const uint32_t rb = kPerT * tid + u;
+    const uint32_t c = rb < nb ? hist[nb - 1 - rb] : 0u;
+    if (run < need && need <= run + c) {
+      sh[0] = nb - 1 - rb;
+      sh[1] = run;
+      sh[2] = c;
+    }
+    run += c;
+  }
+  __syncthreads();
+  above = sh[1];
+  count = sh[2];
+  const uint32_t b = sh[0];
+  __syncthreads();
+  return b;
+}
+
+// Inverse of order_key for keys of real numbers: the float whose key is `key`.
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
+}
+
+// Fast path (see the file header). Returns true when it wrote the row's output; false (with the
+// output untouched) when the exact path has to run. All decisions are block-uniform.
+// Candidates are score indices in per-warp regions of kFastCand / kWarps slots (the memory of the
+// exact path's candidate buffer); their keys are re-read from the row (L2) when needed.
+__device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool vec, uint32_t* hist, uint32_t* cidx,
+                          uint32_t* bitmap, int32_t* out) {
+  constexpr int kRegion = kFastCand / kWarps;  // candidate slots per warp
+  __shared__ uint32_t part[kWarps], sh[4], f_min, f_max, f_small, f_valid, f_over, wcnt[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (n > kBitmapWords * 32 || 3 * k > 2 * kFastCand / 2) return false;
+  // ---- sample: evenly spaced 128-score blocks, two per warp, loads issued together ----
+  uint32_t* skeys = cidx;  // [kSample]
+  const int nblk = (n + 127) / 128;
+  const int sblk = nblk < kSample / 128 ? nblk : kSample / 128;
+  if (tid == 0) {
+    f_min = 0xFFFFFFFFu;
+    f_max = 0u;
+    f_valid = 0u;
+    f_over = 0u;
+  }
+  __syncthreads();
+  {
+    float4 v[2];
+    int jb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = warp + kWarps * u;
+      jb[u] = i < sblk ? 128 * (i * nblk / sblk) : n;  // i * nblk < 2^16: 32-bit math
+      const int j0 = jb[u] + 4 * lane;
+      if (vec && j0 + 4 <= n) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(row + j0));
+      } else {
+        v[u].x = j0 < n ? __ldg(row + j0) : 0.f;
+        v[u].y = j0 + 1 < n ? __ldg(row + j0 + 1) : 0.f;
+        v[u].z = j0 + 2 < n ? __ldg(row + j0 + 2) : 0.f;
+        v[u].w = j0 + 3 < n ? __ldg(row + j0 + 3) : 0.f;
+      }
+    }
+    uint32_t smin = 0xFFFFFFFFu, smax = 0u, svalid = 0;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = warp + kWarps * u;
+      if (i >= sblk) break;  // warp-uniform
+      const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = jb[u] + 4 * lane + e < n;
+        const uint32_t key = order_key(f[e]);
+        skeys[128 * i + 4 * lane + e] = key;
+        if (ok) {
+          smin = min(smin, key);
+          smax = max(smax, key);
+          ++svalid;
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      smin = min(smin, __shfl_xor_sync(0xffffffffu, smin, o));
+      smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+      svalid += __shfl_xor_sync(0xffffffffu, svalid, o);
+    }
+    if (lane == 0) {
+      atomicMin(&f_min, smin);
+      atomicMax(&f_max, smax);
+      atomicAdd(&f_valid, svalid);
+    }
+  }
+  for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  const uint32_t S = f_valid, lo_s = f_min, hi_s = f_max;
+  // sample rank m whose key becomes tau: about 1.5 k of the row (k itself when the sample is the row)
+  uint32_t m = (uint32_t)(S == (uint32_t)n ? k : ((3LL * k * S + 2LL * n - 1) / (2LL * n)));
+  if (m < 1) m = 1;
+  if (m > S) m = S;
+  // ---- adaptive histogram of the sample -> tau ----
+  {
+    const uint32_t range = hi_s - lo_s;
+    const int bits = 32 - __clz(range);
+    const int shift = bits > 12 ? bits - 12 : 0;
+    const uint32_t nb = (range >> shift) + 1;
+    // only the last sampled block can hold slots past the row's end; they are skipped
+    const int last_valid = 128 * (sblk - 1) + (n - 128 * ((sblk - 1) * nblk / sblk));
+    for (int i = tid; i < 128 * sblk; i += kThreads)
+      if (i < last_valid) atomicAdd(&hist[(skeys[i] - lo_s) >> shift], 1u);
+    __syncthreads();
+    uint32_t above, count;
+    const uint32_t b = bin_from_top(hist, nb, m, part, sh, above, count);
+    if (b == 0xFFFFFFFFu) return false;
+    if (tid == 0) sh[3] = lo_s + (b << shift);
+  }
+  const int words = (n + 31) / 32;
+  for (int i = tid; i < words; i += kThreads) bitmap[i] = 0;
+  __syncthreads();
+  const uint32_t tau = sh[3];
+  // key >= tau  <=>  score >= ftau for every number (NaN fails both, its key being 0 < tau unless
+  // tau is 0; then ftau is NaN, no candidate is found and the exact path runs)
+  const float ftau = key_to_float(tau);
+  // ---- filter: the index of every score >= ftau goes to this warp's region ----
+  uint32_t* region = cidx + kRegion * warp;
+  uint32_t cnt = 0;  // candidates of this warp so far (warp-uniform)
+  const uint32_t lt = (1u << lane) - 1u;
+  walk_chunk_f(row, c0, c1, vec, [&](int j0, const float (&x)[4], uint32_t valid) {
+    uint32_t cm = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cm |= (x[e] >= ftau) ? (1u << e) : 0u;
+    cm &= valid;
+    const uint32_t m0 = __ballot_sync(0xffffffffu, cm & 1u), m1 = __ballot_sync(0xffffffffu, cm & 2u);
+    const uint32_t m2 = __ballot_sync(0xffffffffu, cm & 4u), m3 = __ballot_sync(0xffffffffu, cm & 8u);
+    const uint32_t p0 = (uint32_t)__popc(m0), p1 = (uint32_t)__popc(m1), p2 = (uint32_t)__popc(m2);
+    uint32_t o = cnt + (uint32_t)__popc(m0 & lt);
+    if ((cm & 1u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0;
+    o = cnt + p0 + (uint32_t)__popc(m1 & lt);
+    if ((cm & 2u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0 + 1;
+    o = cnt + p0 + p1 + (uint32_t)__popc(m2 & lt);
+    if ((cm & 4u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0 + 2;
+    o = cnt + p0 + p1 + p2 + (uint32_t)__popc(m3 & lt);
+    if ((cm & 8u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0 + 3;
+    cnt += p0 + p1 + p2 + (uint32_t)__popc(m3);
+  });
+  if (lane == 0) {
+    wcnt[warp] = cnt;
+    if (cnt > (uint32_t)kRegion) atomicOr(&f_over, 1u);
+    atomicAdd(&f_valid, cnt);  // f_valid now counts S + candidates
+  }
+  __syncthreads();
+  const uint32_t C = f_valid - S;
+  if (f_over || C < (uint32_t)k) return false;
+  // ---- select: the k-th largest composite (key, -index) among the candidates ----
+  // Thread t owns slots t + 512 u (u < 16): their keys are loaded once, all loads in flight
+  // together, and kept in registers (0 marks an empty slot: no candidate has key 0, tau > 0).
+  constexpr int kPer = kFastCand / kThreads;
+  uint32_t ckey[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + kThreads * u;
+    const bool used = (uint32_t)(i % kRegion) < wcnt[i / kRegion];
+    ckey[u] = used ? __float_as_uint(__ldg(row + cidx[i])) : 0u;
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int i = tid + kThreads * u;
+    const bool used = (uint32_t)(i % kRegion) < wcnt[i / kRegion];
+    ckey[u] = used ? order_key(__uint_as_float(ckey[u])) : 0u;
+  }
+  // Bins over [tau, sample max]; larger keys share the top bin (the map stays monotone, so the
+  // selection stays exact: only the few candidates of the threshold bin are compared in full).
+  uint64_t T;
+  {
+    const uint32_t lo = tau, hi = hi_s > tau ? hi_s : tau;
+    const uint32_t range = hi - lo;
+    const int bits = 32 - __clz(range);
+    const int shift = bits > 12 ? bits - 12 : 0;
+    const uint32_t nb = (range >> shift) + 1;
+    auto bin_of = [&](uint32_t key) -> uint32_t {
+      const uint32_t b = (key - lo) >> shift;
+      return b < nb ? b : nb - 1;
+    };
+    for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
+    if (tid == 0) f_small = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (ckey[u] != 0u) atomicAdd(&hist[bin_of(ckey[u])], 1u);
+    __syncthreads();
+    uint32_t above, count;
+    const uint32_t b = bin_from_top(hist, nb, (uint32_t)k, part, sh, above, count);
+    if (b == 0xFFFFFFFFu || count > (uint32_t)kSmallSort) return false;
+    // gather the threshold bin's candidates (behind the first kSelBins bins of hist)
+    uint64_t* small = reinterpret_cast<uint64_t*>(hist + kSelBins);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (ckey[u] != 0u && bin_of(ckey[u]) == b) {
+        const uint32_t j = cidx[tid + kThreads * u];
+        small[atomicAdd(&f_small, 1u)] = ((uint64_t)ckey[u] << 32) | (uint32_t)(0xFFFFFFFFu - j);
+      }
+    __syncthreads();
+    int P = 2;
+    while (P < (int)count) P <<= 1;
+    for (int i = (int)count + tid; i < P; i += kThreads) small[i] = 0;
+    __syncthreads();
+    // bitonic sort, descending
+    for (int size = 2; size <= P; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < (P >> 1); i += kThreads) {
+          const int a = 2 * stride * (i / stride) + (i % stride), c = a + stride;
+          const bool desc = (a & size) == 0;
+          const uint64_t x = small[a], y = small[c];
+          if ((x < y) == desc) {
+            small[a] = y;
+            small[c] = x;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    T = small[(uint32_t)k - above - 1];
+  }
+  // ---- write: mark the kept candidates, then emit set bits in index order ----
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    if (ckey[u] != 0u) {
+      const uint32_t j = cidx[tid + kThreads * u];
+      if ((((uint64_t)ckey[u] << 32) | (uint32_t)(0xFFFFFFFFu - j)) >= T) atomicOr(&bitmap[j >> 5], 1u << (j & 31));
+    }
+  __syncthreads();
+  const int wpt = (words + kThreads - 1) / kThreads;  // bitmap words per thread
+  const int w0 = tid * wpt;
+  const int w1 = w0 + wpt < words ? w0 + wpt : words;
+  uint32_t nset = 0;
+  for (int w = w0; w < w1; ++w) nset += (uint32_t)__popc(bitmap[w]);
+  uint32_t total;
+  uint32_t o = block_excl_scan(nset, part, total);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = bitmap[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1;
+      if (o < (uint32_t)k) out[o] = 32 * w + b;
+      ++o;
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 2)
     topk_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ kvlen, int32_t k,
                 int32_t* __restrict__ idx, int32_t* err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw);              // [kBins]
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw + kBins * 4);  // [kMaxCand]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + kOffHist);   // [kBins]
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw + kOffCand);   // [kMaxCand]
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + kOffBitmap);  // [kBitmapWords]
   __shared__ uint32_t red_min[kWarps], red_max[kWarps], warp_cnt[kWarps], warp_off[kWarps];
   __shared__ uint32_t scan_part[kWarps];
   __shared__ uint32_t sel_bin, sel_above, sel_count, n_cand;
@@ -104,6 +451,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int c0 = warp * per;
   const int c1 = c0 + per < ni ? c0 + per : ni;
 
+  if (fast_topk(row, ni, k, c0, c1, vec, hist, reinterpret_cast<uint32_t*>(cand), bitmap, out)) return;
+
+  // ================================ exact path ==================================================
   // ---- pass 0: key range --------------------------------------------------------------------
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
   walk_chunk(row, c0, c1, vec, [&](int, const uint32_t (&key)[4], uint32_t valid) {
@@ -347,6 +697,10 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* kvlen, i
                         int32_t* idx, int32_t* err, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(topk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, topk::kSmem);
+  if (e != cudaSuccess) return e;
+  // the same shared-memory carve-out as the indexer and sparse-MLA kernels, so the SMs keep their
+  // configuration between the three launches of a step
+  e = cudaFuncSetAttribute(topk::topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   topk::topk_kernel<<<T, topk::kThreads, topk::kSmem, stream>>>(scores, ld, kvlen, k, idx, err);
   return cudaGetLastError();

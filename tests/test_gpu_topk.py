@@ -60,3 +60,28 @@ def test_bad_length_flagged():
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     hs_topk(s, kl, 8, idx, err)
     assert hs_check_flag(err) & 0x02
+
+
+@pytest.mark.parametrize("k", [256, 2048])
+def test_sampled_threshold_rows(k):
+    """Rows shaped for the sampled-threshold path (and its fall-backs): indexer-like positive scores,
+    sorted ramps (all winners at one end), heavy upper tails, a few huge outliers, rows barely
+    longer than k, and rows whose whole length fits the sample."""
+    rng = np.random.default_rng(11 + k)
+    ld = 70000
+    rows = []
+    rows.append((rng.random(ld) * 40).astype(np.float32))                      # positive, like ReLU sums
+    rows.append(np.arange(ld, dtype=np.float32))                               # ascending ramp
+    rows.append(np.arange(ld, 0, -1).astype(np.float32))                       # descending ramp
+    rows.append(rng.exponential(1.0, ld).astype(np.float32) ** 3)             # heavy upper tail
+    r = rng.standard_normal(ld).astype(np.float32)
+    r[rng.choice(ld, 50, replace=False)] = 1e30                                # a few huge outliers
+    rows.append(r)
+    rows.append(np.round(rng.standard_normal(ld) * 2).astype(np.float32))      # few distinct values
+    s = np.stack(rows + [rng.standard_normal(ld).astype(np.float32) for _ in range(6)])
+    T = s.shape[0]
+    kvlen = rng.integers(16384, ld + 1, size=T).astype(np.int32)
+    kvlen[-4:] = [k + 1, k + 37, 4096, 4097]
+    got = _run(s, kvlen, k)
+    ref = oracle.topk(s.astype(np.float64), kvlen, k)
+    assert np.array_equal(got, ref)
