@@ -12,11 +12,12 @@
 // Keys sit on the MMA's M (TMEM lanes), so each epilogue thread owns one key and does the ReLU,
 // the weighted head sum and the causal mask in registers, then writes one coalesced score.
 //
-// Roles (320 threads): warp 0 issues TMA loads (query tile once, two 64-key pages per stage),
-// warp 1 allocates TMEM and issues tcgen05.mma (e4m3 x e4m3 -> fp32, M=128, N=256, K=32),
-// warps 2..9 drain the two TMEM accumulators: each warp owns its 32-lane quarter and a 128-column
-// slice, reads the slice into registers, hands the accumulator back to the MMA at once, and only then
-// does the arithmetic (so the tensor pipe never waits for the ALU work of the tile before).
+// Roles (576 threads): warp 0 issues TMA loads (query tile once, two 64-key pages per stage, and
+// the pages' key scales), warp 1 allocates TMEM and issues tcgen05.mma (e4m3 x e4m3 -> fp32,
+// M=128, N=256, K=32), warps 2..17 drain the two TMEM accumulators: each warp owns its 32-lane
+// quarter and a 64-column slice, reads the slice into registers, hands the accumulator back to
+// the MMA at once, and only then does the arithmetic (so the tensor pipe never waits for the ALU
+// work of the tile before). Four epilogue warps per scheduler keep its ALU work issuing.
 #include "common.cuh"
 
 namespace hs {
@@ -25,11 +26,15 @@ namespace indexer {
 constexpr int kBlockM = 128;   // keys per tile (two pages)
 constexpr int kN = 256;        // (token, head) columns per group
 constexpr int kStages = 6;
-constexpr int kEpiWarps = 8;    // two per TMEM lane quarter; 10 warps leave 168 registers a thread
+constexpr int kEpiWarps = 16;   // four per TMEM lane quarter, each a 64-column slice
 constexpr int kSlice = kN * 4 / kEpiWarps;  // accumulator columns per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxG = 32;      // tokens per group when Hi = 8
 constexpr int kMaxTpc = 64;    // tiles per CTA and segment
+// Key scales of tile i sit in slot i % kScaleRing. The TMA warp refills a slot for tile i + 8 only
+// after MMA of tile i + 2 released stage (i + 8) % kStages, and that MMA waited for every epilogue
+// warp to have read tile i (scales included) from the accumulator it reuses: 8 slots never race.
+constexpr int kScaleRing = kStages + 2;
 
 struct Params {
   int32_t T, B, Hi, Di;
@@ -45,8 +50,19 @@ struct Params {
   int64_t ld;
   int32_t* err;
   int32_t tiles_per_cta;
-  int32_t scale_prefetch;  // k_scale is 16-byte aligned: pull each page's 64 scales into L2 early
+  int32_t scale_tma;  // k_scale is 16-byte aligned: the TMA warp copies each page's 64 scales to smem
 };
+
+// Shared-memory load issued where it is written: the folded head weights are the same for every
+// tile, and letting the compiler hoist them out of the tile loop makes it spill them to local
+// memory and reload them from there on every tile.
+__device__ __forceinline__ float4 lds_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
 
 template <int DI, int HI>
 struct Cfg {
@@ -63,7 +79,8 @@ struct Cfg {
   static constexpr int kOffSeg = kOffTok + 4 * kMaxG * 4;     // int32 x 4 x kMaxG
   static constexpr int kOffBlk = kOffSeg + 4 * kMaxG * 4;   // int32 [kMaxG][2 * kMaxTpc]
   static constexpr int kOffLim = kOffBlk + kMaxG * 2 * kMaxTpc * 4;  // int32 [kMaxG][kMaxG]
-  static constexpr int kOffBar = kOffLim + kMaxG * kMaxG * 4;
+  static constexpr int kOffScale = kOffLim + kMaxG * kMaxG * 4;  // float [kScaleRing][kBlockM]
+  static constexpr int kOffBar = kOffScale + kScaleRing * kBlockM * 4;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmem = kOffMisc + 64 + 1024;          // + alignment slack
@@ -88,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* sSegHi = sSegLo + kMaxG;                      // one past the last tile
   int32_t* sBlk = (int32_t*)(smem + C::kOffBlk);         // physical page of each of the CTA's pages
   int32_t* sLim = (int32_t*)(smem + C::kOffLim);         // [segment][token]: visible keys, 0 = other request
+  float* sScale = (float*)(smem + C::kOffScale);         // key scales of the tiles in flight
   uint64_t* bars = (uint64_t*)(smem + C::kOffBar);
   uint64_t* full = bars;                                 // [kStages]
   uint64_t* empty = bars + kStages;                      // [kStages]
@@ -221,13 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t bytes = 0;
             for (int pg = 0; pg < 2; ++pg) {
               blk[pg] = sBlk[s * 2 * kMaxTpc + 2 * (kt - sSegLo[s]) + pg];
-              if (blk[pg] >= 0) bytes += 64 * DI;
+              if (blk[pg] >= 0) bytes += 64 * DI + (p.scale_tma ? 64 * 4 : 0);
             }
             mbar_arrive_expect_tx(&full[st], bytes);
             for (int pg = 0; pg < 2; ++pg)
               if (blk[pg] >= 0) {
                 tma_load_2d(sK + st * C::kTileBytes + pg * 64 * DI, &map_k, &full[st], 0, blk[pg] * 64);
-                if (p.scale_prefetch) bulk_prefetch_l2(p.k_scale + (int64_t)blk[pg] * 64, 64 * 4);
+                if (p.scale_tma)
+                  bulk_g2s(sScale + (it % kScaleRing) * kBlockM + pg * 64, p.k_scale + (int64_t)blk[pg] * 64, 64 * 4,
+                           &full[st]);
               }
           }
         }
@@ -287,18 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jn = sSegN[s];                                    // keys of the segment's longest token
         const int32_t* blk_s = sBlk + s * 2 * kMaxTpc - 2 * lo;     // page of (tile kt, half) at 2 kt + half
         const int32_t* lim_s = sLim + s * kMaxG + g0;
-        // key scale of this thread's key in tile kt; < 0 marks a key outside the request
-        auto key_scale = [&](int kt) -> float {
-          const int j = kt * kBlockM + row;
-          if (j >= jn) return -1.f;
-          const int32_t blk = blk_s[2 * kt + (row >> 6)];
-          return blk >= 0 ? __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63)) : -1.f;
-        };
-        float ks = lo < hi ? key_scale(lo) : -1.f;
         for (int kt = lo; kt < hi; ++kt, ++it) {
-          // next tile's key scale, fetched before waiting (its latency overlaps this tile; the
-          // producer has already pulled the scales into L2 together with the keys)
-          const float ks_next = kt + 1 < hi ? key_scale(kt + 1) : -1.f;
           const int b = it & 1;
           const uint32_t aph = (uint32_t)(it >> 1) & 1u;
           const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
@@ -312,19 +321,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t acc[kSlice / 32][32];
 #pragma unroll
           for (int q = 0; q < kSlice / 32; ++q) tmem_ld32(taddr + 32 * q, acc[q]);
+          // key scale of this thread's key (< 0: the key lies outside the request), read before the
+          // accumulator is released (the scale slot's lifetime depends on it)
+          const int j = kt * kBlockM + row;
+          float ks = -1.f;
+          if (j < jn) {
+            const int32_t blk = blk_s[2 * kt + (row >> 6)];
+            if (blk >= 0)
+              ks = p.scale_tma ? sScale[(it % kScaleRing) * kBlockM + row]
+                               : __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63));
+          }
           tmem_wait_ld();
           // the slice is in registers: the accumulator may take the next MMA
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[b]);
-          const int j = kt * kBlockM + row;
 #pragma unroll
           for (int k = 0; k < kTok; ++k) {
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
             for (int h = 0; h < HI; h += 4) {
               const int c = k * HI + h;
-              const float4 wv = *reinterpret_cast<const float4*>(wsl + c);
+              const float4 wv = lds_f4(wsl + c);
               const float x0 = __uint_as_float(acc[c / 32][c % 32]);
               const float x1 = __uint_as_float(acc[c / 32][c % 32 + 1]);
               const float x2 = __uint_as_float(acc[c / 32][c % 32 + 2]);
@@ -335,7 +353,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ks >= 0.f && j < lim_s[k])
               srow[(int64_t)k * p.ld + (int64_t)kt * kBlockM] = ks * ((a0 + a1) + (a2 + a3));
           }
-          ks = ks_next;
         }
       }
     }
@@ -400,7 +417,7 @@ cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t s
   if (tpc < 8) tpc = 8;
   if (tpc > 64) tpc = 64;
   p.tiles_per_cta = (int)tpc;
-  p.scale_prefetch = ((uintptr_t)a->k_scale & 15) == 0 ? 1 : 0;
+  p.scale_tma = ((uintptr_t)a->k_scale & 15) == 0 ? 1 : 0;
   int splits = (int)((tiles_max + tpc - 1) / tpc);
   if (splits < 1) splits = 1;
   if (groups == 0) return cudaSuccess;
