@@ -7,10 +7,13 @@
 // Since both scales are positive, s = k_scale[j] * sum_h (w*q_scale)[t,h] * max(0, <q, k>):
 // the GEMM runs on raw e4m3 codes and the scales are applied in the epilogue.
 //
-// Work split: a CTA owns one group of 256/Hi consecutive query tokens (so the MMA's N is
-// tokens x heads = 256) and a contiguous range of 128-key tiles of each request in the group.
-// Keys sit on the MMA's M (TMEM lanes), so each epilogue thread owns one key and does the ReLU,
-// the weighted head sum and the causal mask in registers, then writes one coalesced score.
+// Work split: query tokens are taken in groups of 256/Hi consecutive tokens (so the MMA's N is
+// tokens x heads = 256); a group's work is the 128-key tiles of each request in it. The kernel is
+// persistent: one CTA per SM takes an equal share of all (group, tile) units (every CTA derives
+// the per-group tile counts from the token lengths itself), so requests of very different
+// lengths still keep every SM busy to the end. Keys sit on the MMA's M (TMEM lanes), so each
+// epilogue thread owns one key and does the ReLU, the weighted head sum and the causal mask in
+// registers, then writes one coalesced score.
 //
 // Roles (576 threads): warp 0 issues TMA loads (query tile once, two 64-key pages per stage, and
 // the pages' key scales), warp 1 allocates TMEM and issues tcgen05.mma (e4m3 x e4m3 -> fp32,
@@ -30,7 +33,6 @@ constexpr int kEpiWarps = 16;   // four per TMEM lane quarter, each a 64-column 
 constexpr int kSlice = kN * 4 / kEpiWarps;  // accumulator columns per epilogue warp
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxG = 32;      // tokens per group when Hi = 8
-constexpr int kMaxTpc = 64;    // tiles per CTA and segment
 // Key scales of tile i sit in slot i % kScaleRing. The TMA warp refills a slot for tile i + 8 only
 // after MMA of tile i + 2 released stage (i + 8) % kStages, and that MMA waited for every epilogue
 // warp to have read tile i (scales included) from the accumulator it reuses: 8 slots never race.
@@ -38,6 +40,8 @@ constexpr int kScaleRing = kStages + 2;
 
 struct Params {
   int32_t T, B, Hi, Di;
+  int32_t t_base;          // first query token of this launch (calls with many groups are split)
+  int32_t ngroups;         // token groups of this launch (<= kMaxGroups)
   const float* q_scale;
   const float* weights;
   const float* k_scale;
@@ -49,19 +53,42 @@ struct Params {
   float* scores;
   int64_t ld;
   int32_t* err;
-  int32_t tiles_per_cta;
   int32_t scale_tma;  // k_scale is 16-byte aligned: the TMA warp copies each page's 64 scales to smem
 };
+
+// Work map: every CTA stages the launch's token lengths in chunks, derives each group's number
+// of key tiles (sum over its requests of ceil(longest visible length / 128)) and their exclusive
+// prefix sum. CTA c then takes the units [c U / C, (c + 1) U / C) of the flattened
+// (group, request, tile) list, which it walks in pieces of at most kMaxPieceTiles tiles.
+constexpr int kMaxGroups = 2048;
+constexpr int kMaxPieceTiles = 512;
+constexpr int kMapChunk = 512;     // tokens staged per step of the work map (a multiple of every G)
 
 // Shared-memory load issued where it is written: the folded head weights are the same for every
 // tile, and letting the compiler hoist them out of the tile loop makes it spill them to local
 // memory and reload them from there on every tile.
-__device__ __forceinline__ float4 lds_f4(const float* p) {
+// The address is a shared-window address plus a compile-time byte offset, which the instruction
+// takes as its immediate (no per-load address arithmetic).
+template <int kOffset>
+__device__ __forceinline__ float4 lds_f4(uint32_t saddr) {
   float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4 + %5];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(smem_u32(p)));
+               : "r"(saddr), "n"(kOffset));
   return v;
+}
+
+// Calls f(std::integral_constant<int, i>) for i = 0 .. N-1 (compile-time indices).
+template <int I>
+struct IntC {
+  static constexpr int value = I;
+};
+template <int N, int I = 0, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  if constexpr (I < N) {
+    f(IntC<I>{});
+    static_for<N, I + 1>(f);
+  }
 }
 
 template <int DI, int HI>
@@ -73,18 +100,42 @@ struct Cfg {
   static constexpr uint32_t kSBO = 8 * DI;                    // one 8-row swizzle atom
   static constexpr int kKSteps = DI / 32;                     // K = 32 per e4m3 MMA
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffK = kQBytes;                       // (the work map's staging aliases it)
   static constexpr int kOffW = kOffK + kStages * kTileBytes;
-  static constexpr int kOffTok = kOffW + kN * 4;              // int32 x 4 x kMaxG
-  static constexpr int kOffSeg = kOffTok + 4 * kMaxG * 4;     // int32 x 4 x kMaxG
-  static constexpr int kOffBlk = kOffSeg + 4 * kMaxG * 4;   // int32 [kMaxG][2 * kMaxTpc]
-  static constexpr int kOffLim = kOffBlk + kMaxG * 2 * kMaxTpc * 4;  // int32 [kMaxG][kMaxG]
-  static constexpr int kOffScale = kOffLim + kMaxG * kMaxG * 4;  // float [kScaleRing][kBlockM]
-  static constexpr int kOffBar = kOffScale + kScaleRing * kBlockM * 4;
+  static constexpr int kOffTok = kOffW + kN * 4;              // int32 x 2 x kMaxG
+  static constexpr int kOffSeg = kOffTok + 2 * kMaxG * 4;     // int32 x 6 x kMaxG
+  static constexpr int kOffBlk = kOffSeg + 6 * kMaxG * 4;     // int32 [2 * kMaxPieceTiles]
+  static constexpr int kOffLim = kOffBlk + 2 * kMaxPieceTiles * 4;  // int32 [kMaxG][kMaxG]
+  static constexpr int kOffScale = kOffLim + kMaxG * kMaxG * 4;     // float [kScaleRing][kBlockM]
+  static constexpr int kOffGroup = kOffScale + kScaleRing * kBlockM * 4;  // int32 [kMaxGroups + 1]
+  static constexpr int kOffBar = kOffGroup + (kMaxGroups + 4) * 4;
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmem = kOffMisc + 64 + 1024;          // + alignment slack
+  static constexpr int kSmem = kOffMisc + 256 + 1024;         // + alignment slack
+  static_assert(2 * kMapChunk * 4 <= kStages * kTileBytes, "work-map staging fits the K stages");
 };
+
+// Block-wide exclusive prefix sum of one value per thread; also returns the total.
+__device__ __forceinline__ int32_t block_scan_excl(int32_t v, int32_t* part, int32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) part[warp] = incl;
+  __syncthreads();
+  int32_t before = 0, all = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int32_t x = part[w];
+    before += w < warp ? x : 0;
+    all += x;
+  }
+  __syncthreads();
+  total = all;
+  return before + incl - v;
+}
 
 template <int DI, int HI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,16 +147,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
-  float* sW = (float*)(smem + C::kOffW);                 // (w * q_scale) [G][HI]
+  float* sW = (float*)(smem + C::kOffW);                 // (w * q_scale) [G][HI] of the current group
   int32_t* sTokN = (int32_t*)(smem + C::kOffTok);        // visible keys per token (0 = skip)
   int32_t* sTokSeg = sTokN + kMaxG;                      // segment of each token (-1 = none)
   int32_t* sSegReq = (int32_t*)(smem + C::kOffSeg);      // request of each segment
   int32_t* sSegN = sSegReq + kMaxG;                      // max visible keys in the segment
-  int32_t* sSegLo = sSegN + kMaxG;                       // first tile of this CTA
+  int32_t* sSegBase = sSegN + kMaxG;                     // first unit of the segment within its group
+  int32_t* sSegLo = sSegBase + kMaxG;                    // first tile of the current piece
   int32_t* sSegHi = sSegLo + kMaxG;                      // one past the last tile
-  int32_t* sBlk = (int32_t*)(smem + C::kOffBlk);         // physical page of each of the CTA's pages
+  int32_t* sSegPg = sSegHi + kMaxG;                      // offset of the segment's pages in sBlk
+  int32_t* sBlk = (int32_t*)(smem + C::kOffBlk);         // physical page of each of the piece's pages
   int32_t* sLim = (int32_t*)(smem + C::kOffLim);         // [segment][token]: visible keys, 0 = other request
   float* sScale = (float*)(smem + C::kOffScale);         // key scales of the tiles in flight
+  int32_t* sGroupOff = (int32_t*)(smem + C::kOffGroup);  // exclusive prefix of the groups' tiles (+ total)
   uint64_t* bars = (uint64_t*)(smem + C::kOffBar);
   uint64_t* full = bars;                                 // [kStages]
   uint64_t* empty = bars + kStages;                      // [kStages]
@@ -113,40 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_empty = acc_full + 2;                    // [2]
   uint64_t* q_full = acc_empty + 2;
   uint64_t* mma_done = q_full + 1;
-  int32_t* misc = (int32_t*)(smem + C::kOffMisc);        // [0] nseg, [1] abort, [2] tmem base
+  int32_t* misc = (int32_t*)(smem + C::kOffMisc);
+  // misc: [0] nseg, [1] abort, [2] tmem base, [3] piece group, [4] piece first unit (group-local),
+  //       [5] piece end unit, [6] group changed, [7..] scan partials
   volatile int32_t* abort_flag = misc + 1;
+  int32_t* scan_part = misc + 8;                         // [kThreads / 32]
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int group = blockIdx.x, split = blockIdx.y;
-  const int t0 = group * G;
+  const int64_t nmax = p.ld < (int64_t)p.bt_stride * 64 ? p.ld : (int64_t)p.bt_stride * 64;
 
-  // ---------------- setup: token metadata, folded weights, segments, barriers, TMEM -------------
-  if (tid < G) {
-    const int t = t0 + tid;
-    int32_t n = 0, r = -1;
-    if (t < p.T) {
-      r = p.token_req[t];
-      n = p.token_kvlen[t];
-      const int64_t nmax = p.ld < (int64_t)p.bt_stride * 64 ? p.ld : (int64_t)p.bt_stride * 64;
-      if (r < 0 || r >= p.B) {
-        flag_error(p.err, HS_FLAG_BAD_INDEX);
-        n = 0;
-      } else if (n < 0 || (int64_t)n > nmax) {
-        flag_error(p.err, HS_FLAG_BAD_LENGTH);
-        n = 0;
-      }
-    }
-    sTokN[tid] = n;
-    sTokSeg[tid] = (n > 0) ? r : -1;  // request for now; turned into a segment id below
-  }
-  if (tid < G * HI) {
-    // folded weight w * q_scale; heads 4m+2, 4m+3 take their ReLU as x + |x| = 2 max(x, 0), so
-    // their weight carries the factor 1/2 (exact)
-    const int g = tid / HI, h = tid % HI, t = t0 + g;
-    const float half = (h & 2) ? 0.5f : 1.f;
-    sW[tid] = (t < p.T) ? half * (p.weights[(int64_t)t * HI + h] * p.q_scale[(int64_t)t * HI + h]) : 0.f;
-  }
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
@@ -162,75 +192,203 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[1] = 0;
   }
   if (warp == 1) tmem_alloc((uint32_t*)&misc[2], 512);
-  __syncthreads();
-  if (tid == 0) {
-    int nseg = 0;
-    for (int g = 0; g < G; ++g) {
-      const int r = sTokSeg[g];
-      if (r < 0) continue;
-      int s = 0;
-      while (s < nseg && sSegReq[s] != r) ++s;
-      if (s == nseg) {
-        sSegReq[s] = r;
-        sSegN[s] = 0;
-        ++nseg;
-      }
-      sTokSeg[g] = s;
-      if (sTokN[g] > sSegN[s]) sSegN[s] = sTokN[g];
-    }
-    for (int s = 0; s < nseg; ++s) {
-      const int tiles = (sSegN[s] + kBlockM - 1) / kBlockM;
-      const int lo = split * p.tiles_per_cta;
-      int hi = lo + p.tiles_per_cta;
-      if (hi > tiles) hi = tiles;
-      sSegLo[s] = lo;
-      sSegHi[s] = hi > lo ? hi : lo;
-    }
-    misc[0] = nseg;
-  }
-  __syncthreads();
-  // keys token g may see while the CTA scores segment s (0 when g belongs to another request)
-  for (int i = tid; i < misc[0] * G; i += kThreads) {
-    const int sg = i / G, g = i % G;
-    sLim[sg * kMaxG + g] = sTokSeg[g] == sg ? sTokN[g] : 0;
-  }
-  // stage this CTA's block-table entries (2 pages per tile) so no warp waits on them later
-  for (int s = 0; s < misc[0]; ++s) {
-    const int r = sSegReq[s];
-    const int npg = 2 * (sSegHi[s] - sSegLo[s]);
-    for (int i = tid; i < npg; i += kThreads) {
-      const int page = 2 * sSegLo[s] + i;
-      int32_t b = -1;
-      if (page * 64 < sSegN[s]) {
-        b = p.block_table[(int64_t)r * p.bt_stride + page];
-        if (b < 0 || (int64_t)b >= p.nblk) {
-          flag_error(p.err, HS_FLAG_BAD_BLOCK);
-          b = -1;
-        }
-      }
-      sBlk[s * 2 * kMaxTpc + i] = b;
-    }
-  }
-  __syncthreads();
-  tc_fence_after();
-  const int nseg = misc[0];
-  const uint32_t tmem = (uint32_t)misc[2];
-  int total = 0;
-  for (int s = 0; s < nseg; ++s) total += sSegHi[s] - sSegLo[s];
 
-  if (total > 0) {
+  // ---------------- work map: tiles per group and their prefix sums ----------------------------
+  {
+    int32_t* cReq = (int32_t*)sK;         // staged tokens of one chunk
+    int32_t* cLen = cReq + kMapChunk;
+    const int Tl = p.T - p.t_base < p.ngroups * G ? p.T - p.t_base : p.ngroups * G;  // tokens of this launch
+    for (int c0 = 0; c0 < p.ngroups * G; c0 += kMapChunk) {
+      __syncthreads();
+      for (int i = tid; i < kMapChunk; i += kThreads) {
+        const int t = c0 + i;
+        int32_t r = -1, n = 0;
+        if (t < Tl) {
+          r = p.token_req[p.t_base + t];
+          n = p.token_kvlen[p.t_base + t];
+          if (r < 0 || r >= p.B || n < 0 || (int64_t)n > nmax) n = 0;  // flagged by the piece setup
+        }
+        cReq[i] = r;
+        cLen[i] = n;
+      }
+      __syncthreads();
+      for (int gl = tid; gl < kMapChunk / G; gl += kThreads) {
+        const int g = c0 / G + gl;
+        if (g >= p.ngroups) break;
+        int32_t tiles = 0;
+        for (int i = 0; i < G; ++i) {
+          const int32_t r = cReq[gl * G + i], n = cLen[gl * G + i];
+          if (n <= 0) continue;
+          bool first = true;
+          int32_t m = n;
+          for (int j = 0; j < G; ++j) {
+            if (j == i || cReq[gl * G + j] != r || cLen[gl * G + j] <= 0) continue;
+            if (j < i) first = false;
+            m = cLen[gl * G + j] > m ? cLen[gl * G + j] : m;
+          }
+          if (first) tiles += (m + kBlockM - 1) / kBlockM;
+        }
+        sGroupOff[g] = tiles;
+      }
+    }
+    __syncthreads();
+    // exclusive prefix sum over the groups (each thread sums a run of consecutive groups)
+    constexpr int kPer = (kMaxGroups + kThreads - 1) / kThreads;
+    int32_t loc[kPer], sum = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int g = tid * kPer + u;
+      loc[u] = g < p.ngroups ? sGroupOff[g] : 0;
+      sum += loc[u];
+    }
+    int32_t total;
+    int32_t run = block_scan_excl(sum, scan_part, total);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int g = tid * kPer + u;
+      if (g < p.ngroups) sGroupOff[g] = run;
+      run += loc[u];
+    }
+    if (tid == 0) sGroupOff[p.ngroups] = total;
+    __syncthreads();
+  }
+  tc_fence_after();
+  const uint32_t tmem = (uint32_t)misc[2];
+  const int64_t U = sGroupOff[p.ngroups];
+  const int32_t u_lo = (int32_t)(U * blockIdx.x / gridDim.x), u_hi = (int32_t)(U * (blockIdx.x + 1) / gridDim.x);
+  // first group of this CTA: the last group whose prefix is <= u_lo among groups with tiles
+  int32_t cur_g = 0;
+  {
+    int lo = 0, hi = p.ngroups;  // find the largest g with sGroupOff[g] <= u_lo (g < ngroups)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sGroupOff[mid] <= u_lo) lo = mid;
+      else hi = mid;
+    }
+    cur_g = lo;
+  }
+  int32_t cur_u = u_lo;
+  int prev_g = -1;
+  // per-role iteration counters, continued across pieces
+  int it_prod = 0, it_mma = 0, it_epi = 0, q_loads = 0;
+
+  while (cur_u < u_hi) {
+    // skip groups without tiles
+    while (cur_g < p.ngroups - 1 && sGroupOff[cur_g + 1] <= cur_u) ++cur_g;
+    const int32_t g_off = sGroupOff[cur_g], g_tiles = sGroupOff[cur_g + 1] - g_off;
+    const int32_t a = cur_u - g_off;
+    int32_t b = (u_hi < g_off + g_tiles ? u_hi : g_off + g_tiles) - g_off;
+    if (b - a > kMaxPieceTiles) b = a + kMaxPieceTiles;
+    const bool new_group = cur_g != prev_g;
+    const int t0 = cur_g * G;  // group's first token (launch-local)
+
+    // ---------------- piece setup ---------------------------------------------------------------
+    __syncthreads();  // the previous piece is fully consumed (epilogue waited for its last MMA)
+    if (new_group) {
+      if (tid < G) {
+        const int t = t0 + tid;
+        int32_t n = 0, r = -1;
+        if (t < p.ngroups * G && p.t_base + t < p.T) {
+          r = p.token_req[p.t_base + t];
+          n = p.token_kvlen[p.t_base + t];
+          if (r < 0 || r >= p.B) {
+            flag_error(p.err, HS_FLAG_BAD_INDEX);
+            n = 0;
+          } else if (n < 0 || (int64_t)n > nmax) {
+            flag_error(p.err, HS_FLAG_BAD_LENGTH);
+            n = 0;
+          }
+        }
+        sTokN[tid] = n;
+        sTokSeg[tid] = (n > 0) ? r : -1;  // request for now; turned into a segment id below
+      }
+      if (tid < G * HI) {
+        // folded weight w * q_scale; heads 4m+2, 4m+3 take their ReLU as x + |x| = 2 max(x, 0), so
+        // their weight carries the factor 1/2 (exact)
+        const int g = tid / HI, h = tid % HI, t = p.t_base + t0 + g;
+        const float half = (h & 2) ? 0.5f : 1.f;
+        sW[tid] = (t < p.T) ? half * (p.weights[(int64_t)t * HI + h] * p.q_scale[(int64_t)t * HI + h]) : 0.f;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int nseg = 0;
+        for (int g = 0; g < G; ++g) {
+          const int r = sTokSeg[g];
+          if (r < 0) continue;
+          int s2 = 0;
+          while (s2 < nseg && sSegReq[s2] != r) ++s2;
+          if (s2 == nseg) {
+            sSegReq[s2] = r;
+            sSegN[s2] = 0;
+            ++nseg;
+          }
+          sTokSeg[g] = s2;
+          if (sTokN[g] > sSegN[s2]) sSegN[s2] = sTokN[g];
+        }
+        int base = 0;
+        for (int s2 = 0; s2 < nseg; ++s2) {
+          sSegBase[s2] = base;
+          base += (sSegN[s2] + kBlockM - 1) / kBlockM;
+        }
+        misc[0] = nseg;
+      }
+      __syncthreads();
+      // keys token g may see while the CTA scores segment s (0 when g belongs to another request)
+      for (int i = tid; i < misc[0] * G; i += kThreads) {
+        const int sg = i / G, g = i % G;
+        sLim[sg * kMaxG + g] = sTokSeg[g] == sg ? sTokN[g] : 0;
+      }
+    }
+    if (tid == 0) {
+      // the piece's tile range within each segment, and where the segment's pages go in sBlk
+      int pg = 0;
+      for (int s2 = 0; s2 < misc[0]; ++s2) {
+        const int tiles = (sSegN[s2] + kBlockM - 1) / kBlockM;
+        int lo = a - sSegBase[s2], hi = b - sSegBase[s2];
+        lo = lo < 0 ? 0 : (lo > tiles ? tiles : lo);
+        hi = hi < 0 ? 0 : (hi > tiles ? tiles : hi);
+        sSegLo[s2] = lo;
+        sSegHi[s2] = hi;
+        sSegPg[s2] = pg;
+        pg += 2 * (hi - lo);
+      }
+    }
+    __syncthreads();
+    // stage the piece's block-table entries (2 pages per tile) so no warp waits on them later
+    const int nseg = misc[0];
+    for (int s2 = 0; s2 < nseg; ++s2) {
+      const int r = sSegReq[s2];
+      const int npg = 2 * (sSegHi[s2] - sSegLo[s2]);
+      for (int i = tid; i < npg; i += kThreads) {
+        const int page = 2 * sSegLo[s2] + i;
+        int32_t blk = -1;
+        if (page * 64 < sSegN[s2]) {
+          blk = p.block_table[(int64_t)r * p.bt_stride + page];
+          if (blk < 0 || (int64_t)blk >= p.nblk) {
+            flag_error(p.err, HS_FLAG_BAD_BLOCK);
+            blk = -1;
+          }
+        }
+        sBlk[sSegPg[s2] + i] = blk;
+      }
+    }
+    __syncthreads();
+
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer ----------------
       if (lane == 0) {
-        prefetch_tensormap(&map_q);
-        prefetch_tensormap(&map_k);
-        mbar_arrive_expect_tx(q_full, C::kQBytes);
-        tma_load_2d(sQ, &map_q, q_full, 0, t0 * HI);
-        int it = 0;
-        for (int s = 0; s < nseg && !*abort_flag; ++s) {
-          for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
-            const int st = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
+        if (new_group) {
+          if (prev_g < 0) {
+            prefetch_tensormap(&map_q);
+            prefetch_tensormap(&map_k);
+          }
+          mbar_arrive_expect_tx(q_full, C::kQBytes);
+          tma_load_2d(sQ, &map_q, q_full, 0, (p.t_base + t0) * HI);
+        }
+        for (int s2 = 0; s2 < nseg && !*abort_flag; ++s2) {
+          for (int kt = sSegLo[s2]; kt < sSegHi[s2]; ++kt, ++it_prod) {
+            const int st = it_prod % kStages;
+            const uint32_t ph = (uint32_t)(it_prod / kStages) & 1u;
             if (!mbar_wait(&empty[st], ph ^ 1u, p.err)) {
               *abort_flag = 1;
               break;
@@ -238,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t blk[2];
             uint32_t bytes = 0;
             for (int pg = 0; pg < 2; ++pg) {
-              blk[pg] = sBlk[s * 2 * kMaxTpc + 2 * (kt - sSegLo[s]) + pg];
+              blk[pg] = sBlk[sSegPg[s2] + 2 * (kt - sSegLo[s2]) + pg];
               if (blk[pg] >= 0) bytes += 64 * DI + (p.scale_tma ? 64 * 4 : 0);
             }
             mbar_arrive_expect_tx(&full[st], bytes);
@@ -246,14 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (blk[pg] >= 0) {
                 tma_load_2d(sK + st * C::kTileBytes + pg * 64 * DI, &map_k, &full[st], 0, blk[pg] * 64);
                 if (p.scale_tma)
-                  bulk_g2s(sScale + (it % kScaleRing) * kBlockM + pg * 64, p.k_scale + (int64_t)blk[pg] * 64, 64 * 4,
-                           &full[st]);
+                  bulk_g2s(sScale + (it_prod % kScaleRing) * kBlockM + pg * 64, p.k_scale + (int64_t)blk[pg] * 64,
+                           64 * 4, &full[st]);
               }
           }
         }
-        // every issued copy must land before the CTA's shared memory is released
-        mbar_wait(q_full, 0, p.err);
-        for (int i = it > kStages ? it - kStages : 0; i < it; ++i)
+        // every issued copy must land before the CTA's shared memory is reused or released
+        if (new_group) mbar_wait(q_full, (uint32_t)q_loads & 1u, p.err);
+        for (int i = it_prod > kStages ? it_prod - kStages : 0; i < it_prod; ++i)
           mbar_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1u, p.err);
       }
     } else if (warp == 1) {
@@ -262,33 +420,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_e4m3(kBlockM, kN);
         const uint32_t q_addr = smem_u32(sQ);
         const uint32_t k_addr = smem_u32(sK);
-        bool ok = mbar_wait(q_full, 0, p.err);
-        int it = 0;
-        for (int s = 0; s < nseg && ok && !*abort_flag; ++s) {
-          for (int kt = sSegLo[s]; kt < sSegHi[s]; ++kt, ++it) {
-            const int st = it % kStages;
-            const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-            const int b = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(&full[st], ph, p.err) || !mbar_wait(&acc_empty[b], aph ^ 1u, p.err)) {
+        bool ok = !new_group || mbar_wait(q_full, (uint32_t)q_loads & 1u, p.err);
+        for (int s2 = 0; s2 < nseg && ok && !*abort_flag; ++s2) {
+          for (int kt = sSegLo[s2]; kt < sSegHi[s2]; ++kt, ++it_mma) {
+            const int st = it_mma % kStages;
+            const uint32_t ph = (uint32_t)(it_mma / kStages) & 1u;
+            const int bb = it_mma & 1;
+            const uint32_t aph = (uint32_t)(it_mma >> 1) & 1u;
+            if (!mbar_wait(&full[st], ph, p.err) || !mbar_wait(&acc_empty[bb], aph ^ 1u, p.err)) {
               ok = false;
               break;
             }
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < C::kKSteps; ++ks) {
-              const uint64_t a = smem_desc(k_addr + st * C::kTileBytes + ks * 32, 16, C::kSBO, C::kSwizzle);
-              const uint64_t bq = smem_desc(q_addr + ks * 32, 16, C::kSBO, C::kSwizzle);
-              mma_e4m3_ss(tmem + (uint32_t)(b * kN), a, bq, idesc, ks > 0 ? 1u : 0u);
+              const uint64_t da = smem_desc(k_addr + st * C::kTileBytes + ks * 32, 16, C::kSBO, C::kSwizzle);
+              const uint64_t dq = smem_desc(q_addr + ks * 32, 16, C::kSBO, C::kSwizzle);
+              mma_e4m3_ss(tmem + (uint32_t)(bb * kN), da, dq, idesc, ks > 0 ? 1u : 0u);
             }
             mma_commit(&empty[st]);
-            mma_commit(&acc_full[b]);
+            mma_commit(&acc_full[bb]);
           }
         }
         if (!ok) *abort_flag = 1;
-        // all issued MMAs must finish before TMEM is released
-        mma_commit(mma_done);
-        mbar_wait(mma_done, 0, p.err);
       }
     } else {
       // ------------------------------------------------------------ epilogue --------------------
@@ -298,26 +452,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = quad * 32 + lane;  // key of the tile (TMEM lane)
       const int g0 = slice * kTok;       // first token of the slice (group-local)
       static_assert(kSlice % HI == 0 && kSlice % 32 == 0, "slice holds whole tokens");
-      const float* wsl = sW + slice * kSlice;
-      float* const srow = p.scores + (int64_t)(t0 + g0) * p.ld + row;  // used only where lim > 0
-      int it = 0;
+      const uint32_t wsl = smem_u32(sW + slice * kSlice);  // this warp's folded weights
+      float* const srow = p.scores + (int64_t)(p.t_base + t0 + g0) * p.ld + row;  // used only where lim > 0
       bool ok = true;
-      for (int s = 0; s < nseg && ok; ++s) {
-        const int lo = sSegLo[s], hi = sSegHi[s];
-        const int jn = sSegN[s];                                    // keys of the segment's longest token
-        const int32_t* blk_s = sBlk + s * 2 * kMaxTpc - 2 * lo;     // page of (tile kt, half) at 2 kt + half
-        const int32_t* lim_s = sLim + s * kMaxG + g0;
-        for (int kt = lo; kt < hi; ++kt, ++it) {
-          const int b = it & 1;
-          const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-          const bool go = !*abort_flag && warp_wait(&acc_full[b], aph, p.err, lane);
+      for (int s2 = 0; s2 < nseg && ok; ++s2) {
+        const int lo = sSegLo[s2], hi = sSegHi[s2];
+        const int jn = sSegN[s2];                                     // keys of the segment's longest token
+        const int32_t* blk_s = sBlk + sSegPg[s2] - 2 * lo;           // page of (tile kt, half) at 2 kt + half
+        const int32_t* lim_s = sLim + s2 * kMaxG + g0;
+        for (int kt = lo; kt < hi; ++kt, ++it_epi) {
+          const int bb = it_epi & 1;
+          const uint32_t aph = (uint32_t)(it_epi >> 1) & 1u;
+          const bool go = !*abort_flag && warp_wait(&acc_full[bb], aph, p.err, lane);
           if (!__all_sync(0xffffffffu, go)) {
             *abort_flag = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * kN + slice * kSlice);
+          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(bb * kN + slice * kSlice);
           uint32_t acc[kSlice / 32][32];
 #pragma unroll
           for (int q = 0; q < kSlice / 32; ++q) tmem_ld32(taddr + 32 * q, acc[q]);
@@ -328,52 +481,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < jn) {
             const int32_t blk = blk_s[2 * kt + (row >> 6)];
             if (blk >= 0)
-              ks = p.scale_tma ? sScale[(it % kScaleRing) * kBlockM + row]
+              ks = p.scale_tma ? sScale[(it_epi % kScaleRing) * kBlockM + row]
                                : __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63));
           }
           tmem_wait_ld();
           // the slice is in registers: the accumulator may take the next MMA
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[b]);
-#pragma unroll
-          for (int k = 0; k < kTok; ++k) {
+          if (lane == 0) mbar_arrive(&acc_empty[bb]);
+          auto token_score = [&](auto kc) -> float {  // weighted ReLU sum of token kc of the slice
+            constexpr int k = decltype(kc)::value;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int h = 0; h < HI; h += 4) {
-              const int c = k * HI + h;
-              const float4 wv = lds_f4(wsl + c);
+            static_for<HI / 4>([&](auto hc) {
+              constexpr int c = k * HI + 4 * decltype(hc)::value;
+              const float4 wv = lds_f4<4 * c>(wsl);
               const float x0 = __uint_as_float(acc[c / 32][c % 32]);
               const float x1 = __uint_as_float(acc[c / 32][c % 32 + 1]);
               const float x2 = __uint_as_float(acc[c / 32][c % 32 + 2]);
               const float x3 = __uint_as_float(acc[c / 32][c % 32 + 3]);
               ffma2(a0, a1, fmaxf(x0, 0.f), fmaxf(x1, 0.f), wv.x, wv.y);
               ffma2(a2, a3, x2 + fabsf(x2), x3 + fabsf(x3), wv.z, wv.w);
-            }
-            if (ks >= 0.f && j < lim_s[k])
-              srow[(int64_t)k * p.ld + (int64_t)kt * kBlockM] = ks * ((a0 + a1) + (a2 + a3));
-          }
+            });
+            return (a0 + a1) + (a2 + a3);
+          };
+          static_for<kTok>([&](auto kc) {
+            constexpr int k = decltype(kc)::value;
+            const float sc = token_score(kc);
+            if (ks >= 0.f && j < lim_s[k]) srow[(int64_t)k * p.ld + (int64_t)kt * kBlockM] = ks * sc;
+          });
         }
       }
+      if (!ok) *abort_flag = 1;
     }
+    if (new_group) ++q_loads;
+    prev_g = cur_g;
+    cur_u = g_off + b;
+    __syncthreads();
+    if (*abort_flag) break;
   }
-  // ---------------- teardown: wait for outstanding MMAs, release TMEM -------------------------------
+  // ---------------- teardown: every issued MMA has finished, release TMEM ---------------------------
   __syncthreads();
   if (warp == 1) {
+    if (lane == 0) {
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, p.err);
+    }
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 template <int DI, int HI>
-static cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const Params& p, int groups, int splits,
-                            cudaStream_t stream) {
+static cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, Params p, int ctas, cudaStream_t stream) {
   using C = Cfg<DI, HI>;
   auto kern = indexer_kernel<DI, HI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(groups, splits), kThreads, C::kSmem, stream>>>(mq, mk, p);
-  return cudaGetLastError();
+  const int G = C::G;
+  const int groups = (p.T + G - 1) / G;
+  for (int g0 = 0; g0 < groups; g0 += kMaxGroups) {  // each launch balances at most kMaxGroups groups
+    p.t_base = g0 * G;
+    p.ngroups = groups - g0 < kMaxGroups ? groups - g0 : kMaxGroups;
+    kern<<<ctas, kThreads, C::kSmem, stream>>>(mq, mk, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace indexer
@@ -408,21 +582,13 @@ cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t s
   p.scores = a->scores;
   p.ld = a->ld;
   p.err = a->err_flag;
-  const int G = kN / HI;
-  const int groups = (a->T + G - 1) / G;
-  const int64_t keys_max = a->ld < (int64_t)a->bt_stride * 64 ? a->ld : (int64_t)a->bt_stride * 64;
-  const int tiles_max = (int)((keys_max + kBlockM - 1) / kBlockM);
-  // about three CTAs' worth of tiles per SM over the whole grid, 8..64 tiles each
-  int64_t tpc = ((int64_t)groups * tiles_max + 3LL * num_sms - 1) / (3LL * num_sms);
-  if (tpc < 8) tpc = 8;
-  if (tpc > 64) tpc = 64;
-  p.tiles_per_cta = (int)tpc;
+  p.t_base = 0;
+  p.ngroups = 0;
   p.scale_tma = ((uintptr_t)a->k_scale & 15) == 0 ? 1 : 0;
-  int splits = (int)((tiles_max + tpc - 1) / tpc);
-  if (splits < 1) splits = 1;
-  if (groups == 0) return cudaSuccess;
+  if (a->T == 0) return cudaSuccess;
+  const int ctas = num_sms;  // persistent: one CTA per SM, each an equal share of the tiles
 #define HS_IDX_CASE(D, H) \
-  if (DI == D && HI == H) return launch_t<D, H>(mq, mk, p, groups, splits, stream);
+  if (DI == D && HI == H) return launch_t<D, H>(mq, mk, p, ctas, stream);
   HS_IDX_CASE(128, 64)
   HS_IDX_CASE(128, 32)
   HS_IDX_CASE(128, 16)
