@@ -14,7 +14,7 @@ import os
 import torch
 
 __all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
-           "hs_sparse_mla_fwd", "hs_hisparse_resolve", "FLAGS"]
+           "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_hisparse_resolve", "FLAGS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libhs.so")
@@ -45,7 +45,7 @@ class _IndexerArgs(ctypes.Structure):
 class _MlaArgs(ctypes.Structure):
     _fields_ = [("T", _i32), ("H", _i32), ("k", _i32), ("q", _P), ("kv_pool", _P), ("R", _i64), ("idx", _P),
                 ("block_table", _P), ("bt_stride", _i32), ("token_req", _P), ("softmax_scale", _f32),
-                ("out", _P), ("lse", _P), ("err_flag", _P)]
+                ("out", _P), ("lse", _P), ("err_flag", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_uint64)]
 
 
 class _ResolveArgs(ctypes.Structure):
@@ -75,8 +75,10 @@ def load():
         lib.hs_indexer_scores.argtypes = [ctypes.POINTER(_IndexerArgs), _P]
         lib.hs_topk.argtypes = [_P, _i64, _P, _i32, _i32, _P, _P, _P]
         lib.hs_sparse_mla_fwd.argtypes = [ctypes.POINTER(_MlaArgs), _P]
+        lib.hs_sparse_mla_workspace_size.argtypes = [_i32, ctypes.POINTER(ctypes.c_uint64)]
         lib.hs_hisparse_resolve.argtypes = [ctypes.POINTER(_ResolveArgs), _P]
-        for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_hisparse_resolve"):
+        for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
+                  "hs_hisparse_resolve"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -147,10 +149,20 @@ def hs_topk(scores, token_kvlen, k: int, idx, err_flag, stream=None):
     _check(load().hs_topk(_ptr(scores), ld, _ptr(token_kvlen), T, k, _ptr(idx), _ptr(err_flag), _stream(stream)))
 
 
+def hs_sparse_mla_workspace_size(H: int) -> int:
+    """Bytes of workspace hs_sparse_mla_fwd needs for H heads on the current device."""
+    n = ctypes.c_uint64(0)
+    _check(load().hs_sparse_mla_workspace_size(int(H), ctypes.byref(n)))
+    return int(n.value)
+
+
 def hs_sparse_mla_fwd(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=None, block_table=None,
-                      token_req=None, stream=None):
-    """Sparse MLA forward: ``out`` bf16 [T, H, 512] (and ``lse`` float32 [T, H] if given)."""
+                      token_req=None, workspace=None, stream=None):
+    """Sparse MLA forward: ``out`` bf16 [T, H, 512] (and ``lse`` float32 [T, H] if given). With a
+    ``workspace`` (uint8 CUDA tensor of at least hs_sparse_mla_workspace_size(H) bytes) every SM
+    gets an equal share of the work and split queries are merged by log-sum-exp."""
     _dev(q, "q", torch.bfloat16), _dev(kv_pool, "kv_pool", torch.uint8), _dev(idx, "idx", torch.int32)
+    _dev(workspace, "workspace", torch.uint8)
     _dev(out, "out", torch.bfloat16), _dev(err_flag, "err_flag", torch.int32), _dev(lse, "lse", torch.float32)
     _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
     T, H, D = q.shape
@@ -158,7 +170,8 @@ def hs_sparse_mla_fwd(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=
         raise HSError(1, "shape mismatch: q [T,H,576], kv_pool [R,656], idx [T,k], out [T,H,512]")
     a = _MlaArgs(T, H, idx.shape[1], _ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(idx), _ptr(block_table),
                  0 if block_table is None else block_table.shape[1], _ptr(token_req), float(softmax_scale),
-                 _ptr(out), _ptr(lse), _ptr(err_flag))
+                 _ptr(out), _ptr(lse), _ptr(err_flag), _ptr(workspace),
+                 0 if workspace is None else workspace.numel())
     _check(load().hs_sparse_mla_fwd(ctypes.byref(a), _stream(stream)))
 
 

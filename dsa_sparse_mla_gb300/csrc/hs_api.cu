@@ -10,7 +10,8 @@ namespace hs {
 cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t stream, const char** why);
 cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* kvlen, int32_t T, int32_t k, int32_t* idx,
                         int32_t* err, cudaStream_t stream);
-cudaError_t launch_mla(const hs_mla_args* a, cudaStream_t stream, const char** why);
+cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const char** why);
+uint64_t mla_workspace_bytes(int32_t H, int sms);
 cudaError_t launch_resolve(const hs_resolve_args* a, cudaStream_t stream);
 }  // namespace hs
 
@@ -140,10 +141,27 @@ hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream) {
   REQUIRE(!a->block_table || (a->token_req && a->bt_stride >= 1), "block_table needs token_req and bt_stride >= 1");
   REQUIRE((int64_t)a->T * a->H <= INT32_MAX && (int64_t)a->T * a->k <= ((int64_t)1 << 40), "T * H or T * k too large");
   REQUIRE(a->softmax_scale == a->softmax_scale, "softmax_scale is NaN");
-  hs_status st = check_device(nullptr);
+  int sms = 0;
+  hs_status st = check_device(&sms);
   if (st != HS_OK) return st;
+  if (a->workspace) {
+    REQUIRE(aligned16(a->workspace), "workspace must be 16-byte aligned");
+    const uint64_t need = hs::mla_workspace_bytes(a->H, sms);
+    REQUIRE(a->workspace_bytes >= need, "workspace holds %llu bytes; H = %d needs %llu on this device",
+            (unsigned long long)a->workspace_bytes, a->H, (unsigned long long)need);
+  }
   const char* why = nullptr;
-  return launched(hs::launch_mla(a, (cudaStream_t)stream, &why), "hs_sparse_mla_fwd", why);
+  return launched(hs::launch_mla(a, sms, (cudaStream_t)stream, &why), "hs_sparse_mla_fwd", why);
+}
+
+hs_status hs_sparse_mla_workspace_size(int32_t H, uint64_t* bytes) {
+  REQUIRE(bytes, "bytes is NULL");
+  REQUIRE(H >= 1 && H <= 64, "H must be in [1, 64] (got %d)", H);
+  int sms = 0;
+  hs_status st = check_device(&sms);
+  if (st != HS_OK) return st;
+  *bytes = hs::mla_workspace_bytes(H, sms);
+  return ok();
 }
 
 hs_status hs_hisparse_resolve(const hs_resolve_args* a, hs_stream_t stream) {

@@ -52,9 +52,11 @@ constexpr int kOffStage = kQBytes;
 constexpr int kOffValid = kOffStage + 2 * kStageBytes;  // uint8 [2][64]
 constexpr int kOffAlpha = kOffValid + 128;          // float [64]
 constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
+constexpr int kOutHeads = 8;                        // heads per chunk of the staged output
+constexpr int kOffOut = kOffInvL + 256;             // bf16 [kOutHeads][512] output staging
 constexpr int kEmpty = 5;                 // per stage: 4 latent block pairs (one PV M-tile each) + RoPE/P
-constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 10;
-constexpr int kOffBar = kOffInvL + 256;
+constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 12;
+constexpr int kOffBar = kOffOut + kOutHeads * HS_D_LATENT * 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort
 constexpr int kSmem = kOffMisc + 16 + 1024;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
@@ -76,7 +78,21 @@ struct Params {
   __nv_bfloat16* out;
   float* lse;
   int32_t* err;
+  // Work split. Units are (query, 64-row tile) pairs, U = T * tiles per query in total. A CTA
+  // takes the units [c U / C, (c + 1) U / C) (persistent launch, C CTAs) or exactly the units of
+  // query c (one CTA per query). A query whose units span several CTAs leaves, from each, its
+  // softmax-normalised partial output (bf16) and log-sum-exp in a workspace slot (2c for the
+  // CTA's first query, 2c + 1 for its last); mla_merge_kernel combines them.
+  int32_t persistent;
+  int64_t U;
+  __nv_bfloat16* part_out;  // [2C][H][512]
+  float* part_lse;          // [2C][H]
 };
+
+// First unit of CTA c of a persistent launch over U units with C CTAs.
+__host__ __device__ __forceinline__ int64_t unit_begin(int64_t c, int64_t U, int64_t C) { return c * U / C; }
+// CTA of a persistent launch holding unit u: the largest c with unit_begin(c) <= u.
+__device__ __forceinline__ int64_t unit_cta(int64_t u, int64_t U, int64_t C) { return ((u + 1) * C - 1) / U; }
 
 // 8 e4m3 codes (two 32-bit words) -> 8 fp16 values code * scale: the e4m3 -> fp16 conversion is
 // exact, the packed multiply rounds once.
@@ -100,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sValid = smem + kOffValid;
   float* sAlpha = (float*)(smem + kOffAlpha);
   float* sInvL = (float*)(smem + kOffInvL);
+  __nv_bfloat16* sOut = (__nv_bfloat16*)(smem + kOffOut);
   uint64_t* bars = (uint64_t*)(smem + kOffBar);
   uint64_t* full = bars + 0;                 // [2][9] producers wrote dim block b -> QK
   uint64_t* empty = bars + 2 * kBlocks;      // [2][5] PV done with block pair m (m = 4: RoPE/P) -> producers
@@ -111,13 +128,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mma_done = s_full + 7;           // QK issuer's MMAs drained
   uint64_t* pv_drain = s_full + 8;           // PV issuer's MMAs drained
   uint64_t* q_ready = s_full + 9;            // Q converted to fp16 (latent dims) -> QK issuer
+  uint64_t* q_free = s_full + 10;            // QK MMAs of a query finished reading Q -> QK issuer
+  uint64_t* o_free = s_full + 11;            // softmax read O^T of a query -> PV issuer
   uint32_t* misc = (uint32_t*)(smem + kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t = blockIdx.x;
   const int k = p.k;
-  const int ntiles = (k + kRows - 1) / kRows;
+  const int ntq = (k + kRows - 1) / kRows;  // tiles per query
+  // this CTA's units; every role walks them as segments (query, tiles [ta, tb)) in the same order,
+  // and counts tiles globally (gi) for the stage and barrier phases
+  int64_t u0, u1;
+  if (p.persistent) {
+    u0 = unit_begin(blockIdx.x, p.U, gridDim.x);
+    u1 = unit_begin(blockIdx.x + 1, p.U, gridDim.x);
+  } else {
+    u0 = (int64_t)blockIdx.x * ntq;
+    u1 = u0 + ntq;
+  }
+  const int ntot = (int)(u1 - u0);  // tiles of this CTA
 
   if (tid == 0) {
     for (int i = 0; i < 2 * kBlocks; ++i) mbar_init(&full[i], kProdWarps);
@@ -132,6 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(mma_done, 1);
     mbar_init(pv_drain, 1);
     mbar_init(q_ready, 4);
+    mbar_init(q_free, 1);
+    mbar_init(o_free, 4);
     mbar_fence_init();
     misc[1] = 0;
   }
@@ -152,16 +183,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     //   tile i+1: row data loaded into registers
     //   tile i  : dequantised into its stage, block by block, once the stage is free.
     // Loads are volatile so they are issued here and not next to their first use.
-    const int req = p.bt ? p.token_req[t] : 0;
-    const int64_t idx_base = (int64_t)t * k;
     const int sub = lane & 3;          // 16-byte piece of a 64-byte latent block
     const int rlat = lane >> 2;        // row (within the warp's 8) of the latent pieces
     const int rrope = lane >> 3;       // row (within a 4-row half) of the RoPE pieces
-    auto ld_idx = [&](int i) -> int32_t {  // lane rr < 8: index entry of row 8 * warp + rr of tile i
-      const int e = i * kRows + warp * 8 + lane;
-      return (lane < 8 && i < ntiles && e < k) ? ldg_nc_s32(p.idx + idx_base + e) : -1;
+    // lane rr < 8: index entry of row 8 * warp + rr of the CTA's next lookahead tile (tiles are
+    // visited in order: la_q / la_t are that tile's query and tile), and (with a block table) the
+    // request of its query
+    int64_t la_q = u0 / ntq;
+    int la_t = (int)(u0 - la_q * ntq), la_n = 0;
+    auto ld_idx = [&](int32_t& req) -> int32_t {
+      req = 0;
+      const bool live = la_n < ntot;
+      const int64_t q = la_q;
+      const int e = la_t * kRows + warp * 8 + lane;
+      if (++la_t == ntq) {
+        la_t = 0;
+        ++la_q;
+      }
+      ++la_n;
+      if (lane >= 8 || !live) return -1;
+      if (p.bt) req = ldg_nc_s32(p.token_req + q);
+      return e < k ? ldg_nc_s32(p.idx + q * k + e) : -1;
     };
-    auto ld_blk = [&](int32_t j) -> int32_t {  // lanes 0-7: block-table entry of entry j (j itself if none)
+    auto ld_blk = [&](int32_t j, int32_t req) -> int32_t {  // lanes 0-7: block-table entry of entry j (j if none)
       if (lane >= 8 || j < 0 || !p.bt) return j;
       const int32_t page = j >> 6;
       return page < p.bt_stride ? ldg_nc_s32(p.bt + (int64_t)req * p.bt_stride + page) : -1;
@@ -254,20 +298,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // prologue: tile 0 in registers, tile 1 prefetched into L2, tile 2 block entries and tile 3
     // index entries in flight
     {
-      const int32_t j0 = ld_idx(0);
-      my_row = phys_row(j0, ld_blk(j0));
+      int32_t r0;
+      const int32_t j0 = ld_idx(r0);
+      my_row = phys_row(j0, ld_blk(j0, r0));
     }
     ld_rows(my_row);
     int64_t row_next;  // lanes 0-7: physical row of tile i+1 (already prefetched)
     {
-      const int32_t j1 = ld_idx(1);
-      row_next = phys_row(j1, ld_blk(j1));
+      int32_t r1;
+      const int32_t j1 = ld_idx(r1);
+      row_next = phys_row(j1, ld_blk(j1, r1));
       if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
     }
-    int32_t jA = ld_idx(2);
-    int32_t bA = ld_blk(jA);
-    int32_t jB = ld_idx(3);
-    for (int i = 0; i < ntiles; ++i) {
+    int32_t rA, rB;
+    int32_t jA = ld_idx(rA);
+    int32_t bA = ld_blk(jA, rA);  // block-table entries travel with their index entries
+    int32_t jB = ld_idx(rB);
+    for (int i = 0; i < ntot; ++i) {
       if (!publish(i)) break;
       // advance: tile i+1 into registers (from L2), tile i+2 into L2, tile i+3 block entries,
       // tile i+4 index entries
@@ -276,8 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_next = phys_row(jA, bA);
       if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
       jA = jB;
-      bA = ld_blk(jB);
-      jB = ld_idx(i + 4);
+      bA = ld_blk(jB, rB);
+      jB = ld_idx(rB);  // tile i + 4
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ QK issuer =================
@@ -285,13 +332,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_qk = idesc_f16(64, kRows, 0, 0);       // latent dims: fp16
       constexpr uint32_t idesc_qk_rope = idesc_bf16(64, kRows, 0, 0); // RoPE dims: bf16
       prefetch_tensormap(&map_q);
-      mbar_arrive_expect_tx(q_full, kQBytes);
-#pragma unroll 1
-      for (int db = 0; db < 9; ++db) tma_load_2d(sQ + db * kBlk, &map_q, q_full, db * 64, t * p.H);
       const uint32_t q_addr = smem_u32(sQ), st_addr = smem_u32(sStage);
-      bool ok = mbar_wait(q_ready, 0, p.err);
+      bool ok = true;
+      int seg = 0, i = 0;  // segment and global tile counters
 #pragma unroll 1
-      for (int i = 0; i < ntiles && ok; ++i) {
+      for (int64_t u = u0; u < u1 && ok; ++seg) {
+        const int64_t q = u / ntq;
+        const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
+        u = q * ntq + tb;
+        if (seg > 0) {  // the previous query's QK MMAs must have read Q before it is replaced
+          mma_commit(q_free);
+          if (!mbar_wait(q_free, (uint32_t)(seg - 1) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+        }
+        mbar_arrive_expect_tx(q_full, kQBytes);
+#pragma unroll 1
+        for (int db = 0; db < 9; ++db) tma_load_2d(sQ + db * kBlk, &map_q, q_full, db * 64, (int32_t)(q * p.H));
+        if (!mbar_wait(q_ready, (uint32_t)seg & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+      for (int jt = ta; jt < tb; ++jt, ++i) {
         const int s = i & 1;
         const uint32_t ph = (uint32_t)(i >> 1) & 1u;
         if (*abort_flag || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
@@ -318,10 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         mma_commit(&s_full[s]);
       }
+      }
       if (!ok) *abort_flag = 1;
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, p.err);
-      mbar_wait(q_full, 0, p.err);
+      if (seg > 0) mbar_wait(q_full, (uint32_t)(seg - 1) & 1u, p.err);  // the last Q copy has landed
     }
   } else if (warp == kPvWarp) {
     // ================================================================ PV issuer =================
@@ -329,8 +394,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
       const uint32_t st_addr = smem_u32(sStage);
       bool ok = true;
+      int seg = 0, j = 0;  // segment and global tile counters
 #pragma unroll 1
-      for (int j = 0; j < ntiles; ++j) {
+      for (int64_t u = u0; u < u1 && ok; ++seg) {
+        const int64_t q = u / ntq;
+        const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
+        u = q * ntq + tb;
+        // O^T of the previous query must have been read out before it is overwritten
+        if (seg > 0 && !mbar_wait(o_free, (uint32_t)(seg - 1) & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+      for (int jt = ta; jt < tb; ++jt, ++j) {
         if (*abort_flag || !mbar_wait(p_ready, (uint32_t)j & 1u, p.err)) {
           ok = false;
           break;
@@ -344,12 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t a = smem_desc(sa + (uint32_t)(2 * mt * kBlk + kk * 2048), kBlk, 1024, 2);
             const uint64_t b = smem_desc(p_addr + kk * 32, 16, 1024, 2);
-            mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (jt > ta || kk > 0) ? 1u : 0u);
           }
           mma_commit(&empty[(j & 1) * kEmpty + mt]);  // dim blocks 2mt, 2mt+1 may be refilled
         }
         mma_commit(pv_done);
         mma_commit(&empty[(j & 1) * kEmpty + 4]);     // P (the RoPE block) consumed
+      }
       }
       if (!ok) *abort_flag = 1;
       mma_commit(pv_drain);
@@ -363,164 +440,186 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hl = lane & 15, half = lane >> 4;
     const int h = quad * 16 + hl;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    {
-      // Q's latent dims (blocks 0-7) bf16 -> fp16 in place; the RoPE block stays bf16
-      const bool qok = warp_wait(q_full, 0, p.err, lane);
-      bool in_range = true;
-      if (qok) {
-        uint4* q4 = reinterpret_cast<uint4*>(sQ);
-        const int sm_tid = tid - (kThreads - kSmThreads);
-        for (int c = sm_tid; c < 8 * kBlk / 16; c += kSmThreads) {
-          uint4 v = q4[c];
-          uint32_t* w = &v.x;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float lo = __uint_as_float(w[u] << 16), hi = __uint_as_float(w[u] & 0xFFFF0000u);
-            in_range &= fabsf(lo) < kF16Max && fabsf(hi) < kF16Max;
-            const __half2 h2 = __floats2half2_rn(lo, hi);
-            w[u] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          q4[c] = v;
-        }
-      }
-      if (!in_range) flag_error(p.err, HS_FLAG_RANGE);
-      if (!qok) *abort_flag = 1;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_ready);
-    }
-    float m_ref = -INFINITY, l_part = 0.f;
     bool ok = true;
+    int seg = 0, i = 0;  // segment and global tile counters
 #pragma unroll 1
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i & 1;
-      const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-      // every exit decision is taken by all four softmax warps together (no partial barriers)
-      // (the last block barrier also orders the producers' row-validity bytes before the reads below)
-      bool w = !*abort_flag && warp_wait(&s_full[s], ph, p.err, lane) &&
-               warp_wait(&full[s * kBlocks + kBlocks - 1], ph, p.err, lane);
-      if (named_bar_or(1, kSmThreads, !w)) {
-        ok = false;
-        *abort_flag = 1;
-        break;
+    for (int64_t u = u0; u < u1 && ok; ++seg) {
+      const int64_t q = u / ntq;
+      const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
+      u = q * ntq + tb;
+      {
+        // Q's latent dims (blocks 0-7) bf16 -> fp16 in place; the RoPE block stays bf16
+        const bool qok = warp_wait(q_full, (uint32_t)seg & 1u, p.err, lane);
+        bool in_range = true;
+        if (qok) {
+          uint4* q4 = reinterpret_cast<uint4*>(sQ);
+          const int sm_tid = tid - (kThreads - kSmThreads);
+#pragma unroll 4
+          for (int c = sm_tid; c < 8 * kBlk / 16; c += kSmThreads) {
+            uint4 v = q4[c];
+            uint32_t* w = &v.x;
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+              const float lo = __uint_as_float(w[uu] << 16), hi = __uint_as_float(w[uu] & 0xFFFF0000u);
+              in_range &= fabsf(lo) < kF16Max && fabsf(hi) < kF16Max;
+              const __half2 h2 = __floats2half2_rn(lo, hi);
+              w[uu] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            q4[c] = v;
+          }
+        }
+        if (!in_range) flag_error(p.err, HS_FLAG_RANGE);
+        if (!qok) *abort_flag = 1;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_ready);
+      }
+      float m_ref = -INFINITY, l_part = 0.f;
+#pragma unroll 1
+      for (int jt = ta; jt < tb; ++jt, ++i) {
+        const int s = i & 1;
+        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+        // every exit decision is taken by all four softmax warps together (no partial barriers)
+        // (the last block barrier also orders the producers' row-validity bytes before the reads below)
+        bool w = !*abort_flag && warp_wait(&s_full[s], ph, p.err, lane) &&
+                 warp_wait(&full[s * kBlocks + kBlocks - 1], ph, p.err, lane);
+        if (named_bar_or(1, kSmThreads, !w)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        uint32_t xr[32];
+        tmem_ld16x2_32(tmem + lane_base + kColS + 64 * s, xr);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[s]);
+        // logits in log2 units, in place (as float bits); masked rows become -inf
+        float mt = -INFINITY;
+        {
+          const uint4* vld4 = reinterpret_cast<const uint4*>(sValid + s * kRows + 32 * half);
+#pragma unroll
+          for (int q4 = 0; q4 < 2; ++q4) {
+            const uint4 vv = vld4[q4];
+            const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int col = q4 * 16 + c;
+              const bool valid = (w4[c >> 2] >> (8 * (c & 3))) & 0xFFu;
+              const float v = valid ? __uint_as_float(xr[col]) * p.scale_log2 : -INFINITY;
+              xr[col] = __float_as_uint(v);
+              mt = fmaxf(mt, v);
+            }
+          }
+        }
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        const bool need = mt > m_ref + kRescaleThreshold;
+        const float m_new = need ? mt : m_ref;
+        // (the first tile of a query starts O^T afresh: PV does not accumulate into it)
+        const bool any = named_bar_or(1, kSmThreads, need && jt > ta);
+        const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;
+        l_part *= alpha;
+        m_ref = m_new;
+        {
+          // P goes into this stage's RoPE block: QK of the tile has finished reading it (s_full), and
+          // the stage is not rewritten before PV of the tile releases it
+          uint8_t* sPt = sStage + s * kStageBytes + 8 * kBlk;
+          float psum = 0.f;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+              const int c = ch * 8 + 2 * uu;
+              const float x0 = __uint_as_float(xr[c]), x1 = __uint_as_float(xr[c + 1]);
+              const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m_ref);
+              const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m_ref);
+              psum += p0 + p1;
+              const __half2 h2 = __floats2half2_rn(p0, p1);
+              pk[uu] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(sPt + sw128_offset(h, (4 * half + ch) * 16)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          l_part += psum;
+        }
+        // PV of the previous tile must have finished accumulating into O^T before it is rescaled and
+        // before this tile's PV is released. Waiting on every tile (after P is written: P is double
+        // buffered with the stages, so this costs no overlap) keeps this warp at most one phase
+        // behind the barrier, which its parity-based wait requires.
+        if (i > 0 && !warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane)) *abort_flag = 1;
+        // rescale O^T columns of the heads whose reference max moved (after P: fewer live registers)
+        if (any) {
+          if (half == 0) sAlpha[h] = alpha;
+          named_bar(1, kSmThreads);
+          tc_fence_after();
+#pragma unroll 1
+          for (int part = 0; part < 8; ++part) {  // 4 M-tiles x 2 halves of 32 head columns
+            uint32_t o[32];
+            const uint32_t oa = tmem + lane_base + kColO + 32 * part;
+            const float* al = sAlpha + 32 * (part & 1);
+            tmem_ld32(oa, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * al[c]);
+            tmem_st32(oa, o);
+          }
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
+      }
+      // ---- the query's normalisation and output (final, or a partial for the merge) ----
+      if (ok) {
+        const bool w = warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane);
+        if (named_bar_or(1, kSmThreads, !w)) {
+          ok = false;
+          *abort_flag = 1;
+        }
       }
       tc_fence_after();
-      uint32_t xr[32];
-      tmem_ld16x2_32(tmem + lane_base + kColS + 64 * s, xr);
-      tmem_wait_ld();
+      const bool whole = ta == 0 && tb == ntq;
+      const int64_t slot = seg == 0 ? 2 * (int64_t)blockIdx.x : 2 * (int64_t)blockIdx.x + 1;
+      __nv_bfloat16* obase = whole ? p.out + q * p.H * HS_D_LATENT : p.part_out + slot * p.H * HS_D_LATENT;
+      float* lbase = whole ? (p.lse ? p.lse + q * p.H : nullptr) : p.part_lse + slot * p.H;
+      const float l_sum = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+      if (half == 0) {
+        sInvL[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        if (lbase && h < p.H) lbase[h] = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
+      }
+      named_bar(1, kSmThreads);
+      if (ok) {
+        // O^T holds dims on TMEM lanes and heads on columns; the output rows are heads. Each chunk
+        // of 8 heads goes through shared memory ([head][512 dims] bf16) and leaves in coalesced
+        // 16-byte stores.
+        const int sm_tid = tid - (kThreads - kSmThreads);
+#pragma unroll 1
+        for (int h0 = 0; h0 < p.H; h0 += kOutHeads) {
+#pragma unroll
+          for (int mt4 = 0; mt4 < 4; ++mt4) {
+            uint32_t o[8];
+            tmem_ld8(tmem + lane_base + kColO + 64 * mt4 + h0, o);
+            tmem_wait_ld();
+            const int d = mt4 * 128 + quad * 32 + lane;
+#pragma unroll
+            for (int c = 0; c < kOutHeads; ++c)
+              sOut[c * HS_D_LATENT + d] = __float2bfloat16_rn(__uint_as_float(o[c]) * sInvL[h0 + c]);
+          }
+          named_bar(1, kSmThreads);
+          const int nh = p.H - h0 < kOutHeads ? p.H - h0 : kOutHeads;
+          const uint4* src = reinterpret_cast<const uint4*>(sOut);
+          uint4* dst = reinterpret_cast<uint4*>(obase + (int64_t)h0 * HS_D_LATENT);
+          for (int v = sm_tid; v < nh * HS_D_LATENT / 8; v += kSmThreads) dst[v] = src[v];
+          named_bar(1, kSmThreads);
+        }
+      }
+      // O^T has been read out: the next query's first PV may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[s]);
-      // logits in log2 units, in place (as float bits); masked rows become -inf
-      float mt = -INFINITY;
-      {
-        const uint4* vld4 = reinterpret_cast<const uint4*>(sValid + s * kRows + 32 * half);
-#pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          const uint4 vv = vld4[q4];
-          const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int col = q4 * 16 + c;
-            const bool valid = (w4[c >> 2] >> (8 * (c & 3))) & 0xFFu;
-            const float v = valid ? __uint_as_float(xr[col]) * p.scale_log2 : -INFINITY;
-            xr[col] = __float_as_uint(v);
-            mt = fmaxf(mt, v);
-          }
-        }
-      }
-      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-      const bool need = mt > m_ref + kRescaleThreshold;
-      const float m_new = need ? mt : m_ref;
-      const bool any = named_bar_or(1, kSmThreads, need && i > 0);
-      const float alpha = need ? fast_exp2(m_ref - m_new) : 1.f;
-      l_part *= alpha;
-      m_ref = m_new;
-      {
-        // P goes into this stage's RoPE block: QK of the tile has finished reading it (s_full), and
-        // the stage is not rewritten before PV of the tile releases it
-        uint8_t* sPt = sStage + s * kStageBytes + 8 * kBlk;
-        float psum = 0.f;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = ch * 8 + 2 * u;
-            const float x0 = __uint_as_float(xr[c]), x1 = __uint_as_float(xr[c + 1]);
-            const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m_ref);
-            const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m_ref);
-            psum += p0 + p1;
-            const __half2 h2 = __floats2half2_rn(p0, p1);
-            pk[u] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(sPt + sw128_offset(h, (4 * half + ch) * 16)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        l_part += psum;
-      }
-      // PV of the previous tile must have finished accumulating into O^T before it is rescaled and
-      // before this tile's PV is released. Waiting on every tile (after P is written: P is double
-      // buffered with the stages, so this costs no overlap) keeps this warp at most one phase
-      // behind the barrier, which its parity-based wait requires.
-      if (i > 0 && !warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane)) *abort_flag = 1;
-      // rescale O^T columns of the heads whose reference max moved (after P: fewer live registers)
-      if (any) {
-        if (half == 0) sAlpha[h] = alpha;
-        named_bar(1, kSmThreads);
-        tc_fence_after();
-#pragma unroll 1
-        for (int part = 0; part < 8; ++part) {  // 4 M-tiles x 2 halves of 32 head columns
-          uint32_t o[32];
-          const uint32_t oa = tmem + lane_base + kColO + 32 * part;
-          const float* al = sAlpha + 32 * (part & 1);
-          tmem_ld32(oa, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * al[c]);
-          tmem_st32(oa, o);
-        }
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready);
-    }
-    // ---- final normalisation and output ----
-    if (ok && ntiles > 0) {
-      const bool w = warp_wait(pv_done, (uint32_t)(ntiles - 1) & 1u, p.err, lane);
-      if (named_bar_or(1, kSmThreads, !w)) {
-        ok = false;
-        *abort_flag = 1;
-      }
-    }
-    tc_fence_after();
-    const float l_sum = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
-    if (half == 0) {
-      sInvL[h] = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      if (p.lse && h < p.H)
-        p.lse[(int64_t)t * p.H + h] = l_sum > 0.f ? (m_ref + log2f(l_sum)) * kLn2 : -INFINITY;
-    }
-    named_bar(1, kSmThreads);
-    if (ok && ntiles > 0) {
-#pragma unroll 1
-      for (int part = 0; part < 8; ++part) {  // 4 M-tiles (128 dims each) x 2 halves of 32 heads
-        uint32_t o[32];
-        const int mt4 = part >> 1, h0 = 32 * (part & 1);
-        tmem_ld32(tmem + lane_base + kColO + 64 * mt4 + h0, o);
-        tmem_wait_ld();
-        const int d = mt4 * 128 + quad * 32 + lane;
-        __nv_bfloat16* dst = p.out + ((int64_t)t * p.H + h0) * HS_D_LATENT + d;
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (h0 + c < p.H)
-            dst[(int64_t)c * HS_D_LATENT] = __float2bfloat16_rn(__uint_as_float(o[c]) * sInvL[h0 + c]);
-      }
-    } else if (ntiles == 0) {
-      for (int hh = 0; hh < p.H; ++hh)
-        for (int d = quad * 32 + lane; d < HS_D_LATENT; d += 128)
-          p.out[((int64_t)t * p.H + hh) * HS_D_LATENT + d] = __float2bfloat16_rn(0.f);
+      if (lane == 0) mbar_arrive(o_free);
     }
   }
   __syncthreads();
@@ -530,9 +629,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Combines the partial outputs of every query whose units were split between CTAs of a
+// persistent launch: with partial (O_s, lse_s) per CTA s, lse = ln sum_s exp(lse_s) and
+// out = sum_s exp(lse_s - lse) O_s (each O_s is already normalised by its own softmax sum).
+// One CTA per query; queries held by a single CTA were written by mla_kernel and are skipped.
+constexpr int kMergeThreads = 512;
+constexpr int kMaxParts = 8;
+__global__ void __launch_bounds__(kMergeThreads)
+    mla_merge_kernel(const Params p, int32_t C) {
+  const int64_t q = blockIdx.x;
+  const int ntq = (p.k + kRows - 1) / kRows;
+  const int64_t ca = unit_cta(q * ntq, p.U, C), cb = unit_cta(q * ntq + ntq - 1, p.U, C);
+  if (ca == cb) return;
+  __shared__ float w[kMaxParts][64];  // merge weight of each part and head
+  __shared__ float lse_tot[64];
+  __shared__ int64_t base[kMaxParts];  // element offset of each part's slot in part_out
+  const int nparts = (int)(cb - ca + 1);
+  if (nparts > kMaxParts) {  // cannot happen for launch sizes the host chooses; never silently wrong
+    if (threadIdx.x == 0) flag_error(p.err, HS_FLAG_BAD_STATE);
+    return;
+  }
+  if (threadIdx.x < nparts) {
+    // slot of CTA c for this query: its first query -> 2c, else its last -> 2c + 1
+    const int64_t c = ca + threadIdx.x;
+    const int64_t sl = unit_begin(c, p.U, C) / ntq == q ? 2 * c : 2 * c + 1;
+    base[threadIdx.x] = sl;
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < p.H; h += kMergeThreads) {
+    float m = -INFINITY;
+    for (int s = 0; s < nparts; ++s) m = fmaxf(m, p.part_lse[base[s] * p.H + h]);
+    float z = 0.f;
+    for (int s = 0; s < nparts; ++s) {
+      const float l = p.part_lse[base[s] * p.H + h];
+      const float e = (m == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - m);
+      w[s][h] = e;
+      z += e;
+    }
+    for (int s = 0; s < nparts; ++s) w[s][h] = z > 0.f ? w[s][h] / z : 0.f;
+    lse_tot[h] = z > 0.f ? m + __logf(z) : -INFINITY;
+  }
+  __syncthreads();
+  if (p.lse)
+    for (int h = threadIdx.x; h < p.H; h += kMergeThreads) p.lse[q * p.H + h] = lse_tot[h];
+  // 8 output values (16 bytes) per vector; a thread's vectors are loaded together, then combined
+  constexpr int kVec = HS_D_LATENT / 8;
+  const int nvec = p.H * kVec;
+  for (int v0 = threadIdx.x; v0 < nvec; v0 += 4 * kMergeThreads) {
+    float acc[4][8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
+    for (int s = 0; s < nparts; ++s) {
+      const __nv_bfloat16* src = p.part_out + base[s] * p.H * HS_D_LATENT;
+      uint4 x[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int v = v0 + b * kMergeThreads;
+        x[b] = v < nvec ? ldg_nc_v4(src + 8 * (int64_t)v) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int v = v0 + b * kMergeThreads;
+        const float ws = v < nvec ? w[s][v / kVec] : 0.f;
+        const uint32_t xs[4] = {x[b].x, x[b].y, x[b].z, x[b].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[b][2 * e] += ws * __uint_as_float(xs[e] << 16);
+          acc[b][2 * e + 1] += ws * __uint_as_float(xs[e] & 0xFFFF0000u);
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int v = v0 + b * kMergeThreads;
+      if (v >= nvec) continue;
+      uint4 o;
+      uint32_t* os = &o.x;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[b][2 * e], acc[b][2 * e + 1]);
+        os[e] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(p.out + q * p.H * HS_D_LATENT + 8 * (int64_t)v) = o;
+    }
+  }
+}
+
 }  // namespace mla
 
-cudaError_t launch_mla(const hs_mla_args* a, cudaStream_t stream, const char** why) {
+// Workspace of the persistent launch on a device with `sms` SMs: two partial slots per CTA.
+uint64_t mla_workspace_bytes(int32_t H, int sms) {
+  return (uint64_t)2 * sms * H * (HS_D_LATENT * 2 + 4);
+}
+
+cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const char** why) {
   using namespace mla;
   CUtensorMap mq;
   if (!encode_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->q, HS_D_QK, (uint64_t)a->T * a->H, HS_D_QK * 2, 64, 64,
@@ -554,10 +746,40 @@ cudaError_t launch_mla(const hs_mla_args* a, cudaStream_t stream, const char** w
   p.out = reinterpret_cast<__nv_bfloat16*>(a->out);
   p.lse = a->lse;
   p.err = a->err_flag;
+  p.persistent = 0;
+  p.U = 0;
+  p.part_out = nullptr;
+  p.part_lse = nullptr;
   if (a->T == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  mla_kernel<<<a->T, kThreads, kSmem, stream>>>(mq, p);
+  const int ntq = (a->k + kRows - 1) / kRows;
+  const int64_t U = (int64_t)a->T * ntq;
+  // One CTA per query keeps every SM busy when the queries fill whole waves; otherwise (fewer
+  // queries than SMs, or a last wave mostly empty) the persistent split pays for its per-query
+  // set-up at the split points and for the merge. The split is used when one CTA per query would
+  // leave more than a quarter of the SM-time of its waves idle.
+  const int64_t waves = (a->T + sms - 1) / sms;
+  const bool split = a->workspace && 4 * (int64_t)a->T < 3 * waves * sms;
+  if (!split) {  // one CTA per query
+    mla_kernel<<<a->T, kThreads, kSmem, stream>>>(mq, p);
+    return cudaGetLastError();
+  }
+  // persistent: one CTA per SM, each an equal share of the units; at most 4 CTAs per query, so
+  // a query is split into at most 5 parts (tiny batches use fewer CTAs)
+  int64_t C64 = sms;
+  if (C64 > U) C64 = U;
+  if (C64 > 4LL * a->T) C64 = 4LL * a->T;
+  const int C = (int)C64;
+  p.persistent = 1;
+  p.U = U;
+  p.part_out = reinterpret_cast<__nv_bfloat16*>(a->workspace);
+  p.part_lse = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a->workspace) +
+                                        (uint64_t)2 * sms * a->H * HS_D_LATENT * 2);
+  mla_kernel<<<C, kThreads, kSmem, stream>>>(mq, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  mla_merge_kernel<<<a->T, kMergeThreads, 0, stream>>>(p, C);
   return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@ import dataclasses
 import numpy as np
 import torch
 
-from . import (hs_hisparse_resolve, hs_indexer_scores, hs_sparse_mla_fwd, hs_topk)
+from . import (hs_hisparse_resolve, hs_indexer_scores, hs_sparse_mla_fwd, hs_sparse_mla_workspace_size, hs_topk)
 from .inputs import HiSparseWorkload, Workload
 
 
@@ -60,6 +60,8 @@ class HotPath:
         self.out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # sparse-MLA scratch: every SM gets an equal share of the (query, tile) work
+        self.workspace = torch.empty(hs_sparse_mla_workspace_size(w.H), dtype=torch.uint8, device=dev)
 
     def indexer(self, stream=None):
         d = self.dw
@@ -72,7 +74,7 @@ class HotPath:
     def mla(self, stream=None):
         d = self.dw
         hs_sparse_mla_fwd(d.q_mla, d.kv_pool, self.idx, d.w.softmax_scale, self.out, self.err, lse=self.lse,
-                          block_table=d.block_table, token_req=d.token_req, stream=stream)
+                          block_table=d.block_table, token_req=d.token_req, workspace=self.workspace, stream=stream)
 
     def step(self, stream=None):
         self.indexer(stream)
@@ -115,6 +117,7 @@ class DeviceHiSparse:
         self.out = torch.empty((B, hw.H, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((B, hw.H), dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.workspace = torch.empty(hs_sparse_mla_workspace_size(hw.H), dtype=torch.uint8, device=device)
 
     def resolve(self, step: int, stream=None):
         hs_hisparse_resolve(step, self.idx[step], self.seq_len, self.resident_start, self.block_table,
@@ -123,7 +126,7 @@ class DeviceHiSparse:
 
     def mla(self, step: int, stream=None):
         hs_sparse_mla_fwd(self.q[step], self.kv_pool, self.rows, self.hw.softmax_scale, self.out, self.err,
-                          lse=self.lse, stream=stream)
+                          lse=self.lse, workspace=self.workspace, stream=stream)
 
     def step(self, step: int, stream=None):
         self.resolve(step, stream)

@@ -76,7 +76,7 @@ typedef enum {
 #define HS_D_LATENT 512          /* latent (value) width */
 #define HS_D_ROPE 64             /* RoPE width */
 #define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
-#define HS_ABI_VERSION 1
+#define HS_ABI_VERSION 2
 
 int hs_abi_version(void);
 const char* hs_status_str(hs_status s);
@@ -184,6 +184,15 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  *   block_table   int32 [B, bt_stride] or NULL; token_req int32 [T] (required with block_table)
  *   out           bf16 [T, H, 512]
  *   lse           fp32 [T, H] or NULL
+ *   workspace     NULL: one CTA per query token. Otherwise at least hs_sparse_mla_workspace_size()
+ *                 bytes of 16-byte aligned device memory (contents need no initialisation, and are
+ *                 scratch after the call): when one CTA per query would leave more than a quarter
+ *                 of the SMs' time idle (fewer queries than SMs, or a mostly empty last wave), the
+ *                 call gives every SM an equal share of the (query, 64-row tile) work instead. A query split between SMs leaves per-SM
+ *                 partial results (softmax-normalised bf16 output and log-sum-exp) in the workspace,
+ *                 which a second kernel on the same stream merges by log-sum-exp, as in [P1]
+ *                 「DCP: KVキャッシュもシャーディング」 (partial attention merged across shards). Calls that
+ *                 share a workspace must not overlap on the GPU.
  * ---------------------------------------------------------------------------------------- */
 typedef struct {
   int32_t T, H, k;
@@ -198,9 +207,15 @@ typedef struct {
   uint16_t* out;
   float* lse;
   int32_t* err_flag;
+  void* workspace;           /* NULL, or caller-owned device scratch (see below) */
+  uint64_t workspace_bytes;  /* its size in bytes */
 } hs_mla_args;
 
 hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream);
+
+/* Bytes of workspace hs_sparse_mla_fwd needs for H heads on the current device (it depends on the
+ * device's SM count): 2 * SMs * H * 1028. */
+hs_status hs_sparse_mla_workspace_size(int32_t H, uint64_t* bytes);
 
 /* ------------------------------------------------------------------------------------------
  * hs_hisparse_resolve — Hybrid HiSparse top-k resolve ("mixed residency").

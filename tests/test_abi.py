@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert hs.hs_abi_version() == 1
+    assert hs.hs_abi_version() == 2
     hs.load()
     for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                                  "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
@@ -53,6 +53,8 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     m = hs._MlaArgs()
     m.T, m.H, m.k = 1, 0, 1
     assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1
+    n = ctypes.c_uint64(0)
+    assert L.hs_sparse_mla_workspace_size(0, ctypes.byref(n)) == 1 and b"H must be" in L.hs_last_error()
     r = hs._ResolveArgs()
     r.B, r.k, r.S, r.step = 1, 9, 8, 0                                # k > S
     assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1

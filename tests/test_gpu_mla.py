@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from dsa_sparse_mla_gb300 import HSError, hs_check_flag, hs_sparse_mla_fwd, inputs
+from dsa_sparse_mla_gb300 import HSError, hs_check_flag, hs_sparse_mla_fwd, hs_sparse_mla_workspace_size, inputs
 
 from parity import check_mla
 
@@ -23,7 +23,11 @@ def _rows(n, seed, group_scales=False):
     return inputs.pack_kv_rows(lat, rope, gs)
 
 
-def _run(q_bits, kv, idx, scale, bt=None, req=None):
+def _workspace(H):
+    return torch.empty(hs_sparse_mla_workspace_size(H), dtype=torch.uint8, device="cuda")
+
+
+def _run(q_bits, kv, idx, scale, bt=None, req=None, split=False):
     T, H, _ = q_bits.shape
     q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
     kvt = torch.from_numpy(kv).cuda()
@@ -33,14 +37,18 @@ def _run(q_bits, kv, idx, scale, bt=None, req=None):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     btt = None if bt is None else torch.from_numpy(bt).cuda()
     rt = None if req is None else torch.from_numpy(req).cuda()
-    hs_sparse_mla_fwd(q, kvt, it, scale, out, err, lse=lse, block_table=btt, token_req=rt)
+    ws = _workspace(H) if split else None
+    if ws is not None:
+        ws.fill_(0xFF)   # the workspace needs no initialisation: stale contents must not matter
+    hs_sparse_mla_fwd(q, kvt, it, scale, out, err, lse=lse, block_table=btt, token_req=rt, workspace=ws)
     flag = hs_check_flag(err)
     return out, lse, flag
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("H,k,n", [(64, 2048, 5000), (64, 130, 300), (16, 256, 1024), (64, 64, 64), (1, 1, 1),
                                    (40, 200, 777)])
-def test_random_index_sets(H, k, n):
+def test_random_index_sets(H, k, n, split):
     rng = np.random.default_rng(H * 1000 + k)
     T = 7
     kv = _rows(n, seed=k + n)
@@ -51,10 +59,46 @@ def test_random_index_sets(H, k, n):
         idx[2, 3] = idx[2, 0]                  # duplicate entry
     idx[4, :] = -1                             # empty query
     scale = 1 / math.sqrt(576)
-    out, lse, flag = _run(q, kv, idx, scale)
+    out, lse, flag = _run(q, kv, idx, scale, split=split)
     assert flag == 0
     ref, lref = oracle.sparse_mla(q, kv, idx, scale)
     check_mla(out, lse, ref, lref)
+
+
+@pytest.mark.parametrize("T,k", [(1, 2048), (3, 2048), (157, 512), (40, 256), (64, 1984)])
+def test_work_split_across_sms(T, k):
+    """Equal shares per SM: queries split between SMs (partials merged by log-sum-exp), fewer
+    queries than SMs, batches that are not a multiple of the SM count, a ragged last tile;
+    the result equals the oracle and the one-CTA-per-query path."""
+    n, H = 3000, 64
+    rng = np.random.default_rng(T * 7 + k)
+    kv = _rows(n, seed=T + k)
+    q = inputs.bf16_bits(inputs.Stream(T + 11).sub("q").normal((T, H, 576)))
+    idx = np.stack([rng.integers(0, n, k) for _ in range(T)]).astype(np.int32)
+    idx[0, k // 2:] = -1                       # a query whose second half is padding
+    if T > 2:
+        idx[2, :] = -1                         # an empty query
+    scale = 1 / math.sqrt(576)
+    out, lse, flag = _run(q, kv, idx, scale, split=True)
+    assert flag == 0
+    ref, lref = oracle.sparse_mla(q, kv, idx, scale)
+    check_mla(out, lse, ref, lref)
+    out1, lse1, flag1 = _run(q, kv, idx, scale, split=False)
+    assert flag1 == 0
+    d = (out.float() - out1.float()).abs().max().item()
+    assert d <= 2e-2 * max(1.0, out1.float().abs().max().item())
+
+
+def test_workspace_too_small_rejected():
+    H = 64
+    q = torch.zeros((2, H, 576), dtype=torch.bfloat16, device="cuda")
+    kvt = torch.zeros((8, 656), dtype=torch.uint8, device="cuda")
+    it = torch.zeros((2, 4), dtype=torch.int32, device="cuda")
+    out = torch.empty((2, H, 512), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(hs_sparse_mla_workspace_size(H) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(HSError, match="workspace"):
+        hs_sparse_mla_fwd(q, kvt, it, 0.1, out, err, workspace=ws)
 
 
 def test_distinct_group_scales_and_large_logits():
