@@ -14,7 +14,8 @@ import os
 import torch
 
 __all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
-           "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_hisparse_resolve", "FLAGS"]
+           "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_sparse_mla_fwd_static", "hs_hisparse_resolve",
+           "FLAGS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libhs.so")
@@ -76,9 +77,10 @@ def load():
         lib.hs_topk.argtypes = [_P, _i64, _P, _i32, _i32, _P, _P, _P]
         lib.hs_sparse_mla_fwd.argtypes = [ctypes.POINTER(_MlaArgs), _P]
         lib.hs_sparse_mla_workspace_size.argtypes = [_i32, ctypes.POINTER(ctypes.c_uint64)]
+        lib.hs_sparse_mla_fwd_static.argtypes = [ctypes.POINTER(_MlaArgs), _P]
         lib.hs_hisparse_resolve.argtypes = [ctypes.POINTER(_ResolveArgs), _P]
         for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
-                  "hs_hisparse_resolve"):
+                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -173,6 +175,22 @@ def hs_sparse_mla_fwd(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=
                  _ptr(out), _ptr(lse), _ptr(err_flag), _ptr(workspace),
                  0 if workspace is None else workspace.numel())
     _check(load().hs_sparse_mla_fwd(ctypes.byref(a), _stream(stream)))
+
+
+def hs_sparse_mla_fwd_static(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=None, block_table=None,
+                             token_req=None, stream=None):
+    """hs_sparse_mla_fwd for callers that cannot allocate device memory: the split-work scratch is
+    the library's own fixed device array (see include/hs.h), so no workspace is passed."""
+    _dev(q, "q", torch.bfloat16), _dev(kv_pool, "kv_pool", torch.uint8), _dev(idx, "idx", torch.int32)
+    _dev(out, "out", torch.bfloat16), _dev(err_flag, "err_flag", torch.int32), _dev(lse, "lse", torch.float32)
+    _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
+    T, H, D = q.shape
+    if D != 576 or kv_pool.shape[-1] != 656 or out.shape != (T, H, 512) or idx.shape[0] != T:
+        raise HSError(1, "shape mismatch: q [T,H,576], kv_pool [R,656], idx [T,k], out [T,H,512]")
+    a = _MlaArgs(T, H, idx.shape[1], _ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(idx), _ptr(block_table),
+                 0 if block_table is None else block_table.shape[1], _ptr(token_req), float(softmax_scale),
+                 _ptr(out), _ptr(lse), _ptr(err_flag), None, 0)
+    _check(load().hs_sparse_mla_fwd_static(ctypes.byref(a), _stream(stream)))
 
 
 def hs_hisparse_resolve(step: int, idx, seq_len, resident_start, block_table, host_rows, kv_pool, slot_row,

@@ -58,6 +58,17 @@ hs_status launched(cudaError_t e, const char* what, const char* why) {
 
 }  // namespace
 
+namespace hs {
+// Sets the calling thread's hs_last_error() text; returns s (for calls defined in other files).
+hs_status set_last_error(hs_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+}  // namespace hs
+
 #define REQUIRE(cond, ...) \
   do {                     \
     if (!(cond)) return fail(HS_ERR_INVALID, __VA_ARGS__); \

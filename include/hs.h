@@ -217,6 +217,22 @@ hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream);
  * device's SM count): 2 * SMs * H * 1028. */
 hs_status hs_sparse_mla_workspace_size(int32_t H, uint64_t* bytes);
 
+/* hs_sparse_mla_fwd_static — hs_sparse_mla_fwd for callers that cannot allocate device memory.
+ *
+ * The pages describe no such call; it exists for callers whose device memory belongs to another
+ * allocator (a serving engine's pooled allocator, a runtime with a fixed budget), or that run
+ * where an allocation, which may synchronise the device, is not allowed, and so cannot supply the
+ * workspace. Same arguments and results as hs_sparse_mla_fwd; a->workspace and
+ * a->workspace_bytes are ignored. The scratch is a 24 MiB array inside the library, present on
+ * every GPU that loads it until the process exits; the call allocates nothing.
+ *  - HS_ERR_UNSUPPORTED when the split path would need more than those 24 MiB (H heads on a
+ *    device with so many SMs that 2 * SMs * H * 1028 bytes exceed them).
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current; make it before capturing a stream.
+ *  - All calls share the array and it keeps the last call's contents; nothing in it needs to
+ *    start at zero. Calls that overlap on the GPU race on it and must be ordered by the caller. */
+hs_status hs_sparse_mla_fwd_static(const hs_mla_args* a, hs_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------
  * hs_hisparse_resolve — Hybrid HiSparse top-k resolve ("mixed residency").
  *
