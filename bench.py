@@ -169,7 +169,7 @@ def build_workload(config: int, seed: int, requests: int = 64):
         return inputs.config2(seed=seed, B=requests)
     if config == 3:
         return inputs.config3(seed=seed)
-    raise SystemExit("--config %d: use 1, 2 or 3 for the indexer/top-k/MLA step" % config)
+    raise SystemExit("--config %d: use 1, 2 or 3 for the indexer/top-k/MLA step (4, 5: analysis modes)" % config)
 
 
 def work_of(w):
@@ -335,17 +335,22 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         import oracle
         threads = oracle.num_threads(0)
-        sample = list(range(min(w.T, max(16, 4 * threads))))  # ~10-30 s of CPU work
-        wall_cpu = oracle_sample(w, sample, threads=0)
-        cpu = {"value": round(len(sample) / wall_cpu, 3), "unit": "tokens/s", "cores": min(threads, len(sample)),
-               "kind": "oracle", "sample": "%d query tokens of the same batch (first %d requests), full "
-               "indexer+top-k+MLA in float64; %.1f s wall on %s" % (len(sample), len(sample) // 4 or 1, wall_cpu,
-                                                                     cpu_model())}
+        # bounded sample: whole passes over the batch's query tokens until about 10 s of CPU work
+        sample = list(range(w.T))
+        wall_cpu, passes = 0.0, 0
+        while passes < 4 and (passes == 0 or wall_cpu < 10.0):
+            wall_cpu += oracle_sample(w, sample, threads=0)
+            passes += 1
+        cpu = {"value": round(passes * len(sample) / wall_cpu, 3), "unit": "tokens/s",
+               "cores": min(threads, len(sample)), "kind": "oracle",
+               "sample": "%d pass(es) over the batch's %d query tokens, full indexer+top-k+MLA in float64; "
+                         "%.1f s wall on %s" % (passes, len(sample), wall_cpu, cpu_model())}
 
     line = {"metric": METRIC, "value": round(tokens / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
-            "config": {"workload": w.name, "requests": w.B, "query_tokens": w.T, "ctx": "U{16384..65536}",
+            "config": {"workload": w.name, "requests": w.B, "query_tokens": w.T,
+                       "ctx": "U{16384..65536}" if args.config == 2 else int(w.ctx.max()),
                        "index_heads": w.Hi, "index_dim": w.Di, "topk": w.topk, "mla_heads": w.H, "page": 64,
                        "l2": "256 MB write between timed steps (inputs also > L2)", "parallelism": "dp%d" % world},
             "roofline": roof,
@@ -359,6 +364,116 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------ analysis modes ----
+
+def _timed(fn, flush, reps):
+    """Median device time (ms) of fn() over reps runs, L2 flushed before each, CUDA events."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    fn()
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush.fill_(1)
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return float(statistics.median(a.elapsed_time(b) for a, b in ev))
+
+
+def run_long_prefill(args):
+    """Long prefill from scratch: 131,072 tokens as 64 sequential chunks of 2,048. The cache holds
+    the whole sequence; chunk c's queries are positions 2048 c .. 2048 c + 2047 (their values are
+    the same draws for every chunk, only their positions move). Per chunk: indexer, top-k and sparse
+    MLA times; the indexer-overtakes-attention chunk is reported."""
+    import torch
+    import dsa_sparse_mla_gb300 as hs
+    from dsa_sparse_mla_gb300 import costmodel as cm, inputs
+    from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
+    torch.cuda.set_device(0)
+    hs.load()
+    w = inputs.config4(0)
+    nchunks, clen = 64, 2048
+    w.token_kvlen = (np.arange(clen, dtype=np.int32) + (nchunks - 1) * clen + 1)  # ld for the last chunk
+    dw = DeviceWorkload.from_host(w)
+    hp = HotPath(dw)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    chunks = list(range(0, nchunks, max(1, args.chunk_stride)))
+    if chunks[-1] != nchunks - 1:
+        chunks.append(nchunks - 1)
+    curve = []
+    for c in chunks:
+        kv = np.arange(clen, dtype=np.int32) + c * clen + 1
+        dw.token_kvlen.copy_(torch.from_numpy(kv))
+        w.token_kvlen = kv
+        wk = work_of(w)
+        t_i = _timed(hp.indexer, flush, args.reps)
+        t_k = _timed(hp.topk, flush, args.reps)
+        t_m = _timed(hp.mla, flush, args.reps)
+        curve.append({"chunk": c, "ctx_end": int((c + 1) * clen), "indexer_ms": round(t_i, 4), "topk_ms": round(t_k, 4),
+                      "mla_ms": round(t_m, 4), "indexer_tflops": round(wk["indexer"].flops / (t_i * 1e9), 1)})
+    flag = hs.hs_check_flag(hp.err)
+    cross = next((e["chunk"] for e in curve if e["indexer_ms"] > e["mla_ms"]), None)
+    total_ms = sum(e["indexer_ms"] + e["topk_ms"] + e["mla_ms"] for e in curve)
+    line = {"metric": "long-prefill per-chunk time curve (indexer+top-k+attn)", "workload": "long-prefill-128K",
+            "chunks_timed": len(curve), "chunk_tokens": clen, "curve": curve,
+            "indexer_overtakes_attention_at_chunk": cross,
+            "crossover_ctx_tokens": None if cross is None else (cross + 1) * clen,
+            "tokens_per_s_timed_chunks": round(len(curve) * clen / (total_ms * 1e-3), 1), "device_flag": flag,
+            "reps_per_kernel": args.reps, "l2": "256 MB write before each timed launch", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+
+
+def run_hisparse(args):
+    """HiSparse mixed-residency decode: 32 requests, contexts U{262144..1048576}, the last 4,096
+    tokens resident, older rows in pinned host memory, 4,096 hot slots per request; 50 steps of
+    resolve + sparse MLA over the Zipf(1.1) index stream with 80 % step-to-step overlap."""
+    import torch
+    import dsa_sparse_mla_gb300 as hs
+    from dsa_sparse_mla_gb300 import costmodel as cm, inputs
+    from dsa_sparse_mla_gb300.pipeline import DeviceHiSparse, pinned_uint8
+    torch.cuda.set_device(0)
+    hs.load()
+    t0 = time.perf_counter()
+    hw = inputs.config5(steps=args.hisparse_steps, host_alloc=pinned_uint8)
+    gen_s = time.perf_counter() - t0
+    dh = DeviceHiSparse(hw)
+    stream = torch.cuda.current_stream()
+    steps = hw.idx.shape[0]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    counters = []
+    torch.cuda.synchronize()
+    for st in range(steps):
+        e = ev[st]
+        e[0].record(stream)
+        dh.resolve(st)
+        e[1].record(stream)
+        dh.mla(st)
+        e[2].record(stream)
+        counters.append(dh.counters.sum(0))
+    torch.cuda.synchronize()
+    cnt = torch.stack(counters).cpu().numpy()          # [steps, 3] resident, hit, miss
+    t_res = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    t_mla = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    warm = slice(1, steps)
+    miss_bytes = cnt[:, 2].astype(np.float64) * 656
+    mla_w = cm.mla_work(hw.H, hw.B * hw.k, hw.B)
+    line = {"metric": "HiSparse decode tokens/s (resolve+attn)", "workload": hw.name, "requests": hw.B,
+            "steps": steps, "topk": hw.k, "hot_slots": hw.S, "mla_heads": hw.H,
+            "value": round(hw.B * (steps - 1) / ((t_res[warm] + t_mla[warm]).sum() * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step_warm": round(float((t_res[warm] + t_mla[warm]).mean()), 4),
+            "resolve_ms_warm": round(float(t_res[warm].mean()), 4), "mla_ms_warm": round(float(t_mla[warm].mean()), 4),
+            "step0_cold": {"resolve_ms": round(float(t_res[0]), 4), "mla_ms": round(float(t_mla[0]), 4),
+                           "misses": int(cnt[0, 2]), "host_read_gbs": round(miss_bytes[0] / (t_res[0] * 1e6), 1)},
+            "per_step_warm": {"hits": round(float(cnt[warm, 1].mean()), 1), "misses": round(float(cnt[warm, 2].mean()), 1),
+                              "resident": round(float(cnt[warm, 0].mean()), 1),
+                              "host_read_gbs": round(float((miss_bytes[warm] / (t_res[warm] * 1e6)).mean()), 1)},
+            "mla_hbm_gbs_warm": round(mla_w.bytes / (float(t_mla[warm].mean()) * 1e6), 1),
+            "device_flag": hs.hs_check_flag(dh.err), "inputs_generated_s": round(gen_s, 1), "data": "synthetic",
+            "l2": "no flush (consecutive decode steps)"}
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------------ reference arm -----
@@ -408,10 +523,17 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=2)
     ap.add_argument("--requests", type=int, default=64, help="decode batch size (profiling runs use fewer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chunk-stride", type=int, default=1, help="--config 4: time every n-th chunk")
+    ap.add_argument("--reps", type=int, default=5, help="--config 4: timed launches per kernel and chunk")
+    ap.add_argument("--hisparse-steps", type=int, default=50, help="--config 5: decode steps")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.config == 4:
+        run_long_prefill(args)
+    elif args.config == 5:
+        run_hisparse(args)
     else:
         run_ours(args)
 
