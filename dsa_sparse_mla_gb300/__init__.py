@@ -15,7 +15,7 @@ import torch
 
 __all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
            "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_sparse_mla_fwd_static", "hs_hisparse_resolve",
-           "FLAGS"]
+           "hs_hisparse_touch_host", "FLAGS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libhs.so")
@@ -79,8 +79,9 @@ def load():
         lib.hs_sparse_mla_workspace_size.argtypes = [_i32, ctypes.POINTER(ctypes.c_uint64)]
         lib.hs_sparse_mla_fwd_static.argtypes = [ctypes.POINTER(_MlaArgs), _P]
         lib.hs_hisparse_resolve.argtypes = [ctypes.POINTER(_ResolveArgs), _P]
+        lib.hs_hisparse_touch_host.argtypes = [_i32, _P, _P, _P, _P, _P]
         for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
-                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve"):
+                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve", "hs_hisparse_touch_host"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -211,3 +212,17 @@ def hs_hisparse_resolve(step: int, idx, seq_len, resident_start, block_table, ho
                      _ptr(slot_row), _ptr(slot_token), _ptr(slot_stamp), _ptr(tok2slot), tok2slot.shape[1],
                      _ptr(out_rows), _ptr(counters), _ptr(err_flag))
     _check(load().hs_hisparse_resolve(ctypes.byref(a), _stream(stream)))
+
+
+def hs_hisparse_touch_host(host_rows, seq_len, resident_start, err_flag, stream=None):
+    """Read one word of every host page of each request's offloaded rows, so that the GPU's
+    first-access cost for the host tier is paid here rather than inside a resolve.
+    ``host_rows`` is the int64 CUDA tensor [B] of pointers that hs_hisparse_resolve takes."""
+    for t, n, dt in ((host_rows, "host_rows", torch.int64), (seq_len, "seq_len", torch.int32),
+                     (resident_start, "resident_start", torch.int32), (err_flag, "err_flag", torch.int32)):
+        _dev(t, n, dt)
+    B = host_rows.shape[0]
+    if seq_len.shape[0] != B or resident_start.shape[0] != B:
+        raise HSError(1, "host_rows, seq_len and resident_start must have the same length")
+    _check(load().hs_hisparse_touch_host(B, _ptr(host_rows), _ptr(seq_len), _ptr(resident_start), _ptr(err_flag),
+                                         _stream(stream)))

@@ -3,6 +3,7 @@
 // state between calls except the calling thread's last error text.
 #include <stdarg.h>
 #include <stdio.h>
+#include <unistd.h>
 
 #include "common.cuh"
 
@@ -13,6 +14,8 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* kvlen, i
 cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const char** why);
 uint64_t mla_workspace_bytes(int32_t H, int sms);
 cudaError_t launch_resolve(const hs_resolve_args* a, cudaStream_t stream);
+cudaError_t launch_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,
+                              const int32_t* resident_start, int64_t page, int32_t* err, cudaStream_t stream);
 }  // namespace hs
 
 namespace {
@@ -191,6 +194,20 @@ hs_status hs_hisparse_resolve(const hs_resolve_args* a, hs_stream_t stream) {
   hs_status st = check_device(nullptr);
   if (st != HS_OK) return st;
   return launched(hs::launch_resolve(a, (cudaStream_t)stream), "hs_hisparse_resolve", nullptr);
+}
+
+hs_status hs_hisparse_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,
+                                 const int32_t* resident_start, int32_t* err_flag, hs_stream_t stream) {
+  REQUIRE(B >= 0, "B must be >= 0");
+  REQUIRE(err_flag, "err_flag is NULL");
+  if (B == 0) return ok();
+  REQUIRE(host_rows && seq_len && resident_start, "a required pointer is NULL");
+  hs_status st = check_device(nullptr);
+  if (st != HS_OK) return st;
+  const long page = sysconf(_SC_PAGESIZE);
+  return launched(hs::launch_touch_host(B, host_rows, seq_len, resident_start, page > 0 ? page : 4096, err_flag,
+                                        (cudaStream_t)stream),
+                  "hs_hisparse_touch_host", nullptr);
 }
 
 }  // extern "C"

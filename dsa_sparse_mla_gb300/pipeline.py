@@ -15,7 +15,8 @@ import dataclasses
 import numpy as np
 import torch
 
-from . import (hs_hisparse_resolve, hs_indexer_scores, hs_sparse_mla_fwd, hs_sparse_mla_workspace_size, hs_topk)
+from . import (hs_hisparse_resolve, hs_hisparse_touch_host, hs_indexer_scores, hs_sparse_mla_fwd,
+               hs_sparse_mla_workspace_size, hs_topk)
 from .inputs import HiSparseWorkload, Workload
 
 
@@ -95,7 +96,9 @@ _PINNED_KEEPALIVE: list = []
 
 
 class DeviceHiSparse:
-    """Device state of the mixed-residency decode: pool, block table, LRU state, index stream."""
+    """Device state of the mixed-residency decode: pool, block table, LRU state, index stream.
+    ``touch_host()`` maps the host tier for the GPU once (hs_hisparse_touch_host); a serving
+    system does this when it sets the tier up."""
 
     def __init__(self, hw: HiSparseWorkload, device="cuda"):
         self.hw = hw
@@ -118,6 +121,9 @@ class DeviceHiSparse:
         self.lse = torch.empty((B, hw.H), dtype=torch.float32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self.workspace = torch.empty(hs_sparse_mla_workspace_size(hw.H), dtype=torch.uint8, device=device)
+
+    def touch_host(self, stream=None):
+        hs_hisparse_touch_host(self.host_rows, self.seq_len, self.resident_start, self.err, stream=stream)
 
     def resolve(self, step: int, stream=None):
         hs_hisparse_resolve(step, self.idx[step], self.seq_len, self.resident_start, self.block_table,

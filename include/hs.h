@@ -76,7 +76,7 @@ typedef enum {
 #define HS_D_LATENT 512          /* latent (value) width */
 #define HS_D_ROPE 64             /* RoPE width */
 #define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
-#define HS_ABI_VERSION 2
+#define HS_ABI_VERSION 3
 
 int hs_abi_version(void);
 const char* hs_status_str(hs_status s);
@@ -287,6 +287,29 @@ typedef struct {
 } hs_resolve_args;
 
 hs_status hs_hisparse_resolve(const hs_resolve_args* a, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_hisparse_touch_host — map the host tier for the GPU before the first resolve.
+ *
+ * [P3] 「ハイブリッド HiSparse の技術的実装」 item 2 has the resolve copy missed rows straight from
+ * pinned host memory. The GPU's first read of a host page costs far more than the read itself
+ * (about 0.5 us per 64 KB page on a GB300 with its Grace host, where a 13.6 GB tier took 102 ms
+ * and a second pass 1.4 ms): a resolve whose misses land on pages the GPU has never read waits on
+ * those first reads, and the wait grows with the tier, not with the misses. This call reads one
+ * 4-byte word of every host page holding rows [0, min(resident_start[r], seq_len[r])) of each
+ * request (the rows a resolve may copy), so that this cost is paid once, when the tier is set up.
+ * It changes no memory and nothing a resolve computes.
+ *
+ *   B               requests
+ *   host_rows       device array of B device-accessible pointers (as in hs_resolve_args),
+ *                   each 16-byte aligned, to pinned uint8 [seq_len[r], 656]
+ *   seq_len, resident_start   int32 [B], device
+ *   err_flag        device int32; a misaligned host pointer sets HS_FLAG_BAD_INDEX and its
+ *                   request is skipped
+ * The page size is the host's (sysconf). Asynchronous on `stream`; allocates nothing.
+ * ---------------------------------------------------------------------------------------- */
+hs_status hs_hisparse_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,
+                                 const int32_t* resident_start, int32_t* err_flag, hs_stream_t stream);
 
 #ifdef __cplusplus
 }

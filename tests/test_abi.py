@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert hs.hs_abi_version() == 2
+    assert hs.hs_abi_version() == 3
     hs.load()
     for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                                  "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
@@ -60,6 +60,9 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1
     r.k, r.S = 8, 9000                                                # S too large
     assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1
+    assert L.hs_hisparse_touch_host(-1, None, None, None, None, None) == 1
+    assert L.hs_hisparse_touch_host(2, None, None, None, ctypes.c_void_p(16), None) == 1
+    assert b"NULL" in L.hs_last_error()
 
 
 def test_calls_without_library_fail_loudly(monkeypatch, tmp_path):

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from dsa_sparse_mla_gb300 import hs_check_flag, hs_hisparse_resolve, inputs
+from dsa_sparse_mla_gb300 import hs_check_flag, hs_hisparse_resolve, hs_hisparse_touch_host, inputs
 from dsa_sparse_mla_gb300.pipeline import pinned_uint8
 
 pytestmark = pytest.mark.gpu
@@ -24,7 +24,9 @@ class _State:
         return [torch.from_numpy(a.copy()).cuda() for a in (self.pool, self.stok, self.sstamp, self.t2s)]
 
 
-def _replay(B, k, S, n, res, steps, overlap, seed, resident_every=3):
+def _replay(B, k, S, n, res, steps, overlap, seed, resident_every=3, step_numbers=None, touch=False):
+    """Replays `steps` resolve steps on the GPU and in the oracle and compares everything after each.
+    step_numbers: the (increasing) step value passed at each step; 0, 1, 2, ... by default."""
     rs = n - res
     pages = (n + 63) // 64
     bt = np.full((B, pages), -1, np.int32)
@@ -51,16 +53,20 @@ def _replay(B, k, S, n, res, steps, overlap, seed, resident_every=3):
     out = torch.empty((B, k), dtype=torch.int32, device="cuda")
     cnt = torch.empty((B, 3), dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if touch:
+        hs_hisparse_touch_host(host_ptrs, seq, rsd, err)
+        assert hs_check_flag(err) == 0
     for step in range(steps):
+        snum = step if step_numbers is None else step_numbers[step]
         idx = np.full((B, k), -1, np.int32)
         for r in range(B):
             sel = stream[step, r].tolist()
             if step % resident_every == 0:
                 sel = sorted(sel + [rs + 1, rs + 5 + r])
             idx[r, :len(sel)] = sel
-        o_ref, c_ref = oracle.hisparse_resolve(step, idx, [n] * B, [rs] * B, bt, hosts, ref.pool, slot_row, ref.stok,
+        o_ref, c_ref = oracle.hisparse_resolve(snum, idx, [n] * B, [rs] * B, bt, hosts, ref.pool, slot_row, ref.stok,
                                                ref.sstamp, ref.t2s)
-        hs_hisparse_resolve(step, torch.from_numpy(idx).cuda(), seq, rsd, btd, host_ptrs, dev[0], srd, dev[1], dev[2],
+        hs_hisparse_resolve(snum, torch.from_numpy(idx).cuda(), seq, rsd, btd, host_ptrs, dev[0], srd, dev[1], dev[2],
                             dev[3], out, cnt, err)
         assert hs_check_flag(err) == 0
         assert np.array_equal(out.cpu().numpy(), o_ref), step
@@ -75,6 +81,38 @@ def _replay(B, k, S, n, res, steps, overlap, seed, resident_every=3):
                                                       (4, 100, 100, 3000, 128, 8, 0.9), (1, 2048, 4096, 70000, 4096, 4, 0.8)])
 def test_replay_matches_oracle(B, k, S, n, res, steps, overlap):
     _replay(B, k, S, n, res, steps, overlap, seed=B * 7 + k)
+
+
+def test_replay_wide_stamp_spread():
+    """Step numbers far apart (spreads of up to 2**30 between stamps): the victim order then needs
+    every 4-bit digit of the stamp, not just the lowest ones."""
+    nums = [0, 1, 17, 4099, 70001, 1 << 20, (1 << 24) + 3, (1 << 30) + 5, (1 << 30) + 6, 2**31 - 2]
+    _replay(3, 64, 128, 5000, 256, len(nums), 0.6, seed=11, step_numbers=nums)
+
+
+@pytest.mark.parametrize("B,k,S,n,res,steps,overlap", [(2, 4096, 8192, 60000, 2048, 4, 0.7),
+                                                      (2, 700, 1500, 9000, 512, 5, 0.6)])
+def test_replay_large_and_ragged_slot_counts(B, k, S, n, res, steps, overlap):
+    """S = 8192 (the largest, 8 slots per thread in the sort) and S = 1500 (not a multiple of the
+    block), after a host-tier touch."""
+    _replay(B, k, S, n, res, steps, overlap, seed=B * 5 + S, touch=True)
+
+
+def test_touch_host_changes_nothing_and_flags_misaligned_rows():
+    n = 3000
+    host = pinned_uint8(n * 656).reshape(n, 656)
+    host[:] = (np.arange(n)[:, None] + np.arange(656)[None, :]).astype(np.uint8)
+    before = host.copy()
+    seq = torch.tensor([n, n, n], dtype=torch.int32, device="cuda")
+    rs = torch.tensor([n - 64, 0, n + 50], dtype=torch.int32, device="cuda")  # a normal tier, none, clamped
+    ptrs = torch.tensor([host.ctypes.data] * 3, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hs_hisparse_touch_host(ptrs, seq, rs, err)
+    assert hs_check_flag(err) == 0
+    assert np.array_equal(host, before)
+    bad = torch.tensor([host.ctypes.data + 8], dtype=torch.int64, device="cuda")
+    hs_hisparse_touch_host(bad, seq[:1], rs[:1], err)
+    assert hs_check_flag(err) & 0x01
 
 
 def test_hand_worked_case(golden_dir):
