@@ -52,11 +52,9 @@ constexpr int kOffStage = kQBytes;
 constexpr int kOffValid = kOffStage + 2 * kStageBytes;  // uint8 [2][64]
 constexpr int kOffAlpha = kOffValid + 128;          // float [64]
 constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
-constexpr int kOutHeads = 8;                        // heads per chunk of the staged output
-constexpr int kOffOut = kOffInvL + 256;             // bf16 [kOutHeads][512] output staging
 constexpr int kEmpty = 5;                 // per stage: 4 latent block pairs (one PV M-tile each) + RoPE/P
 constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 12;
-constexpr int kOffBar = kOffOut + kOutHeads * HS_D_LATENT * 2;
+constexpr int kOffBar = kOffInvL + 256;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort
 constexpr int kSmem = kOffMisc + 16 + 1024;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
@@ -116,7 +114,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sValid = smem + kOffValid;
   float* sAlpha = (float*)(smem + kOffAlpha);
   float* sInvL = (float*)(smem + kOffInvL);
-  __nv_bfloat16* sOut = (__nv_bfloat16*)(smem + kOffOut);
   uint64_t* bars = (uint64_t*)(smem + kOffBar);
   uint64_t* full = bars + 0;                 // [2][9] producers wrote dim block b -> QK
   uint64_t* empty = bars + 2 * kBlocks;      // [2][5] PV done with block pair m (m = 4: RoPE/P) -> producers
@@ -592,28 +589,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       named_bar(1, kSmThreads);
       if (ok) {
-        // O^T holds dims on TMEM lanes and heads on columns; the output rows are heads. Each chunk
-        // of 8 heads goes through shared memory ([head][512 dims] bf16) and leaves in coalesced
-        // 16-byte stores.
-        const int sm_tid = tid - (kThreads - kSmThreads);
+        // O^T holds dims on TMEM lanes and heads on columns; the output rows are heads. This thread
+        // owns dim 128 mt + 32 quad + lane of every M-tile mt. Neighbouring lanes swap values so
+        // that each holds two adjacent dims of one head (even lanes: even heads, odd lanes: odd
+        // heads) and writes them with one 4-byte store; a warp's store covers 64 contiguous bytes
+        // of each of two head rows.
+        const int odd = lane & 1;
 #pragma unroll 1
-        for (int h0 = 0; h0 < p.H; h0 += kOutHeads) {
-#pragma unroll
-          for (int mt4 = 0; mt4 < 4; ++mt4) {
-            uint32_t o[8];
-            tmem_ld8(tmem + lane_base + kColO + 64 * mt4 + h0, o);
+        for (int mt4 = 0; mt4 < 4; ++mt4) {
+#pragma unroll 1
+          for (int hh = 0; hh < 2 && 32 * hh < p.H; ++hh) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_base + kColO + 64 * mt4 + 32 * hh, o);
             tmem_wait_ld();
-            const int d = mt4 * 128 + quad * 32 + lane;
+            const int d0 = mt4 * 128 + quad * 32 + (lane & ~1);  // the pair's first dim
 #pragma unroll
-            for (int c = 0; c < kOutHeads; ++c)
-              sOut[c * HS_D_LATENT + d] = __float2bfloat16_rn(__uint_as_float(o[c]) * sInvL[h0 + c]);
+            for (int j = 0; j < 16; ++j) {
+              const float e = __uint_as_float(o[2 * j]), f = __uint_as_float(o[2 * j + 1]);
+              const float mine = odd ? f : e;  // head 2j + odd at this dim
+              const float give = odd ? e : f;  // the other head at this dim
+              const float got = __shfl_xor_sync(0xffffffffu, give, 1);  // this head at the partner's dim
+              const int hd = 32 * hh + 2 * j + odd;
+              if (hd < p.H) {
+                const float il = sInvL[hd];
+                const float lo = odd ? got : mine, hi = odd ? mine : got;
+                *reinterpret_cast<__nv_bfloat162*>(obase + (int64_t)hd * HS_D_LATENT + d0) =
+                    __floats2bfloat162_rn(lo * il, hi * il);
+              }
+            }
           }
-          named_bar(1, kSmThreads);
-          const int nh = p.H - h0 < kOutHeads ? p.H - h0 : kOutHeads;
-          const uint4* src = reinterpret_cast<const uint4*>(sOut);
-          uint4* dst = reinterpret_cast<uint4*>(obase + (int64_t)h0 * HS_D_LATENT);
-          for (int v = sm_tid; v < nh * HS_D_LATENT / 8; v += kSmThreads) dst[v] = src[v];
-          named_bar(1, kSmThreads);
         }
       }
       // O^T has been read out: the next query's first PV may overwrite it
