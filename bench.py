@@ -473,6 +473,7 @@ def run_hisparse(args):
             "resolve_ms_warm": round(float(t_res[warm].mean()), 4), "mla_ms_warm": round(float(t_mla[warm].mean()), 4),
             "step0_cold": {"resolve_ms": round(float(t_res[0]), 4), "mla_ms": round(float(t_mla[0]), 4),
                            "misses": int(cnt[0, 2]), "host_read_gbs": round(miss_bytes[0] / (t_res[0] * 1e6), 1)},
+            "resolve_ms_steps": [round(float(x), 3) for x in t_res[:12]],
             "per_step_warm": {"hits": round(float(cnt[warm, 1].mean()), 1), "misses": round(float(cnt[warm, 2].mean()), 1),
                               "resident": round(float(cnt[warm, 0].mean()), 1),
                               "host_read_gbs": round(float((miss_bytes[warm] / (t_res[warm] * 1e6)).mean()), 1)},
