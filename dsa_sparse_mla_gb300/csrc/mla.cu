@@ -636,18 +636,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Combines the partial outputs of every query whose units were split between CTAs of a
 // persistent launch: with partial (O_s, lse_s) per CTA s, lse = ln sum_s exp(lse_s) and
 // out = sum_s exp(lse_s - lse) O_s (each O_s is already normalised by its own softmax sum).
-// One CTA per query; queries held by a single CTA were written by mla_kernel and are skipped.
-constexpr int kMergeThreads = 512;
+// One CTA per (query, 8 heads); queries held by a single CTA were written by mla_kernel and are
+// skipped. Every part's vectors are loaded before any is combined, so a thread has up to
+// 2 x kMaxParts 16-byte loads in flight.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeHeads = 8;
 constexpr int kMaxParts = 8;
 __global__ void __launch_bounds__(kMergeThreads)
     mla_merge_kernel(const Params p, int32_t C) {
   const int64_t q = blockIdx.x;
+  const int h0 = blockIdx.y * kMergeHeads;
   const int ntq = (p.k + kRows - 1) / kRows;
   const int64_t ca = unit_cta(q * ntq, p.U, C), cb = unit_cta(q * ntq + ntq - 1, p.U, C);
-  if (ca == cb) return;
-  __shared__ float w[kMaxParts][64];  // merge weight of each part and head
-  __shared__ float lse_tot[64];
-  __shared__ int64_t base[kMaxParts];  // element offset of each part's slot in part_out
+  if (ca == cb || h0 >= p.H) return;
+  __shared__ float w[kMaxParts][kMergeHeads];  // merge weight of each part and head
+  __shared__ int64_t base[kMaxParts];          // slot of each part in part_out / part_lse
   const int nparts = (int)(cb - ca + 1);
   if (nparts > kMaxParts) {  // cannot happen for launch sizes the host chooses; never silently wrong
     if (threadIdx.x == 0) flag_error(p.err, HS_FLAG_BAD_STATE);
@@ -656,68 +659,74 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (threadIdx.x < nparts) {
     // slot of CTA c for this query: its first query -> 2c, else its last -> 2c + 1
     const int64_t c = ca + threadIdx.x;
-    const int64_t sl = unit_begin(c, p.U, C) / ntq == q ? 2 * c : 2 * c + 1;
-    base[threadIdx.x] = sl;
+    base[threadIdx.x] = unit_begin(c, p.U, C) / ntq == q ? 2 * c : 2 * c + 1;
   }
   __syncthreads();
-  for (int h = threadIdx.x; h < p.H; h += kMergeThreads) {
+  const int nh = p.H - h0 < kMergeHeads ? p.H - h0 : kMergeHeads;
+  if (threadIdx.x < nh) {
+    const int h = h0 + threadIdx.x;
     float m = -INFINITY;
     for (int s = 0; s < nparts; ++s) m = fmaxf(m, p.part_lse[base[s] * p.H + h]);
     float z = 0.f;
-    for (int s = 0; s < nparts; ++s) {
-      const float l = p.part_lse[base[s] * p.H + h];
-      const float e = (m == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - m);
-      w[s][h] = e;
-      z += e;
+    float e[kMaxParts];
+#pragma unroll
+    for (int s = 0; s < kMaxParts; ++s) {
+      e[s] = 0.f;
+      if (s < nparts) {
+        const float l = p.part_lse[base[s] * p.H + h];
+        e[s] = (m == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - m);
+        z += e[s];
+      }
     }
-    for (int s = 0; s < nparts; ++s) w[s][h] = z > 0.f ? w[s][h] / z : 0.f;
-    lse_tot[h] = z > 0.f ? m + __logf(z) : -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kMaxParts; ++s)
+      if (s < nparts) w[s][threadIdx.x] = z > 0.f ? e[s] / z : 0.f;
+    if (p.lse) p.lse[q * p.H + h] = z > 0.f ? m + __logf(z) : -INFINITY;
   }
   __syncthreads();
-  if (p.lse)
-    for (int h = threadIdx.x; h < p.H; h += kMergeThreads) p.lse[q * p.H + h] = lse_tot[h];
-  // 8 output values (16 bytes) per vector; a thread's vectors are loaded together, then combined
+  // 8 output values (16 bytes) per vector, 64 vectors per head
   constexpr int kVec = HS_D_LATENT / 8;
-  const int nvec = p.H * kVec;
-  for (int v0 = threadIdx.x; v0 < nvec; v0 += 4 * kMergeThreads) {
-    float acc[4][8];
+  constexpr int kPer = kMergeHeads * kVec / kMergeThreads;  // vectors per thread
+  const int nvec = nh * kVec;
+  uint4 x[kMaxParts][kPer];
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
+  for (int s = 0; s < kMaxParts; ++s) {
+    if (s < nparts) {
+      const __nv_bfloat16* src = p.part_out + (base[s] * p.H + h0) * HS_D_LATENT;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[b][e] = 0.f;
-    for (int s = 0; s < nparts; ++s) {
-      const __nv_bfloat16* src = p.part_out + base[s] * p.H * HS_D_LATENT;
-      uint4 x[4];
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int v = v0 + b * kMergeThreads;
-        x[b] = v < nvec ? ldg_nc_v4(src + 8 * (int64_t)v) : make_uint4(0, 0, 0, 0);
+      for (int b = 0; b < kPer; ++b) {
+        const int v = threadIdx.x + b * kMergeThreads;
+        x[s][b] = v < nvec ? ldg_nc_v4(src + 8 * (int64_t)v) : make_uint4(0, 0, 0, 0);
       }
+    }
+  }
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int v = v0 + b * kMergeThreads;
-        const float ws = v < nvec ? w[s][v / kVec] : 0.f;
-        const uint32_t xs[4] = {x[b].x, x[b].y, x[b].z, x[b].w};
+  for (int b = 0; b < kPer; ++b) {
+    const int v = threadIdx.x + b * kMergeThreads;
+    if (v >= nvec) continue;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxParts; ++s) {
+      if (s < nparts) {
+        const float ws = w[s][v / kVec];
+        const uint32_t xs[4] = {x[s][b].x, x[s][b].y, x[s][b].z, x[s][b].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          acc[b][2 * e] += ws * __uint_as_float(xs[e] << 16);
-          acc[b][2 * e + 1] += ws * __uint_as_float(xs[e] & 0xFFFF0000u);
+          acc[2 * e] += ws * __uint_as_float(xs[e] << 16);
+          acc[2 * e + 1] += ws * __uint_as_float(xs[e] & 0xFFFF0000u);
         }
       }
     }
+    uint4 o;
+    uint32_t* os = &o.x;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int v = v0 + b * kMergeThreads;
-      if (v >= nvec) continue;
-      uint4 o;
-      uint32_t* os = &o.x;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[b][2 * e], acc[b][2 * e + 1]);
-        os[e] = *reinterpret_cast<const uint32_t*>(&b2);
-      }
-      *reinterpret_cast<uint4*>(p.out + q * p.H * HS_D_LATENT + 8 * (int64_t)v) = o;
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+      os[e] = *reinterpret_cast<const uint32_t*>(&b2);
     }
+    *reinterpret_cast<uint4*>(p.out + (q * p.H + h0) * HS_D_LATENT + 8 * (int64_t)v) = o;
   }
 }
 
@@ -783,7 +792,8 @@ cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const
   mla_kernel<<<C, kThreads, kSmem, stream>>>(mq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  mla_merge_kernel<<<a->T, kMergeThreads, 0, stream>>>(p, C);
+  mla_merge_kernel<<<dim3((unsigned)a->T, (unsigned)((a->H + kMergeHeads - 1) / kMergeHeads)), kMergeThreads, 0, stream>>>(
+      p, C);
   return cudaGetLastError();
 }
 
