@@ -29,8 +29,7 @@ namespace indexer {
 constexpr int kBlockM = 128;   // keys per tile (two pages)
 constexpr int kN = 256;        // (token, head) columns per group
 constexpr int kStages = 6;
-constexpr int kEpiWarps = 16;   // four per TMEM lane quarter, each a 64-column slice
-constexpr int kSlice = kN * 4 / kEpiWarps;  // accumulator columns per epilogue warp
+constexpr int kEpiWarps = 16;   // four per TMEM lane quarter: two per accumulator, each 128 columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kMaxG = 32;      // tokens per group when Hi = 8
 // Key scales of tile i sit in slot i % kScaleRing. The TMA warp refills a slot for tile i + 8 only
@@ -184,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kEpiWarps);
+      mbar_init(&acc_empty[i], kEpiWarps / 2);  // the warps of that accumulator's parity
     }
     mbar_init(q_full, 1);
     mbar_init(mma_done, 1);
@@ -446,13 +445,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ------------------------------------------------------------ epilogue --------------------
-      constexpr int kTok = kSlice / HI;  // tokens in a warp's column slice
+      // Warps take alternate tiles, so that while one half waits for its TMEM loads the other half
+      // computes: slot = (warp - 2) / 4 in 0..3; the warps of parity slot / 2 drain accumulator
+      // (tile % 2) == parity, each its lane quarter and the columns [col0, col0 + 128) in two
+      // chunks of 64 (chunk 1 is loaded after chunk 0 is reduced; then the accumulator is released).
+      constexpr int kChunk = 64;
+      constexpr int kTok = kChunk / HI;  // tokens in a chunk
+      static_assert(kChunk % HI == 0, "a chunk holds whole tokens");
       const int quad = warp & 3;
-      const int slice = (warp - 2) >> 2;
+      const int slot = (warp - 2) >> 2;
+      const int parity = slot >> 1;
+      const int col0 = (slot & 1) * (kN / 2);
       const int row = quad * 32 + lane;  // key of the tile (TMEM lane)
-      const int g0 = slice * kTok;       // first token of the slice (group-local)
-      static_assert(kSlice % HI == 0 && kSlice % 32 == 0, "slice holds whole tokens");
-      const uint32_t wsl = smem_u32(sW + slice * kSlice);  // this warp's folded weights
+      const int g0 = col0 / HI;          // first token of this warp's columns (group-local)
+      const uint32_t wsl = smem_u32(sW + col0);  // this warp's folded weights
       float* const srow = p.scores + (int64_t)(p.t_base + t0 + g0) * p.ld + row;  // used only where lim > 0
       bool ok = true;
       for (int s2 = 0; s2 < nseg && ok; ++s2) {
@@ -462,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* lim_s = sLim + s2 * kMaxG + g0;
         for (int kt = lo; kt < hi; ++kt, ++it_epi) {
           const int bb = it_epi & 1;
+          if (bb != parity) continue;
           const uint32_t aph = (uint32_t)(it_epi >> 1) & 1u;
           const bool go = !*abort_flag && warp_wait(&acc_full[bb], aph, p.err, lane);
           if (!__all_sync(0xffffffffu, go)) {
@@ -470,10 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(bb * kN + slice * kSlice);
-          uint32_t acc[kSlice / 32][32];
+          const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(bb * kN + col0);
+          uint32_t acc[kChunk / 32][32];
 #pragma unroll
-          for (int q = 0; q < kSlice / 32; ++q) tmem_ld32(taddr + 32 * q, acc[q]);
+          for (int q = 0; q < kChunk / 32; ++q) tmem_ld32(taddr + 32 * q, acc[q]);
           // key scale of this thread's key (< 0: the key lies outside the request), read before the
           // accumulator is released (the scale slot's lifetime depends on it)
           const int j = kt * kBlockM + row;
@@ -484,17 +491,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               ks = p.scale_tma ? sScale[(it_epi % kScaleRing) * kBlockM + row]
                                : __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63));
           }
-          tmem_wait_ld();
-          // the slice is in registers: the accumulator may take the next MMA
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[bb]);
-          auto token_score = [&](auto kc) -> float {  // weighted ReLU sum of token kc of the slice
+          auto token_score = [&](auto cc, auto kc) -> float {  // weighted ReLU sum of token kc of chunk cc
             constexpr int k = decltype(kc)::value;
+            constexpr int wbase = decltype(cc)::value * kChunk;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
             static_for<HI / 4>([&](auto hc) {
               constexpr int c = k * HI + 4 * decltype(hc)::value;
-              const float4 wv = lds_f4<4 * c>(wsl);
+              const float4 wv = lds_f4<4 * (wbase + c)>(wsl);
               const float x0 = __uint_as_float(acc[c / 32][c % 32]);
               const float x1 = __uint_as_float(acc[c / 32][c % 32 + 1]);
               const float x2 = __uint_as_float(acc[c / 32][c % 32 + 2]);
@@ -504,11 +507,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             });
             return (a0 + a1) + (a2 + a3);
           };
-          static_for<kTok>([&](auto kc) {
-            constexpr int k = decltype(kc)::value;
-            const float sc = token_score(kc);
-            if (ks >= 0.f && j < lim_s[k]) srow[(int64_t)k * p.ld + (int64_t)kt * kBlockM] = ks * sc;
-          });
+          float sc[2][kTok];
+          tmem_wait_ld();
+          static_for<kTok>([&](auto kc) { sc[0][decltype(kc)::value] = token_score(IntC<0>{}, kc); });
+#pragma unroll
+          for (int q = 0; q < kChunk / 32; ++q) tmem_ld32(taddr + kChunk + 32 * q, acc[q]);
+          tmem_wait_ld();
+          // both chunks are in registers: the accumulator may take the next MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[bb]);
+          static_for<kTok>([&](auto kc) { sc[1][decltype(kc)::value] = token_score(IntC<1>{}, kc); });
+          if (ks >= 0.f) {
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+              for (int k = 0; k < kTok; ++k) {
+                const int g = c2 * kTok + k;
+                if (j < lim_s[g]) srow[(int64_t)g * p.ld + (int64_t)kt * kBlockM] = ks * sc[c2][k];
+              }
+          }
         }
       }
       if (!ok) *abort_flag = 1;
