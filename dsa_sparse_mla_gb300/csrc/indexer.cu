@@ -211,23 +211,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         cLen[i] = n;
       }
       __syncthreads();
-      for (int gl = tid; gl < kMapChunk / G; gl += kThreads) {
+      // one warp per group, one lane per token (G <= 32): a token adds the tiles of its request's
+      // longest token if no earlier token of the group belongs to the same request
+      static_assert(G <= 32, "a group fits in a warp");
+      for (int gl = warp; gl < kMapChunk / G; gl += kThreads / 32) {
         const int g = c0 / G + gl;
-        if (g >= p.ngroups) break;
-        int32_t tiles = 0;
-        for (int i = 0; i < G; ++i) {
-          const int32_t r = cReq[gl * G + i], n = cLen[gl * G + i];
-          if (n <= 0) continue;
-          bool first = true;
-          int32_t m = n;
-          for (int j = 0; j < G; ++j) {
-            if (j == i || cReq[gl * G + j] != r || cLen[gl * G + j] <= 0) continue;
-            if (j < i) first = false;
-            m = cLen[gl * G + j] > m ? cLen[gl * G + j] : m;
+        if (g >= p.ngroups) break;  // warp-uniform
+        const int32_t r = lane < G ? cReq[gl * G + lane] : -1;
+        const int32_t n = lane < G ? cLen[gl * G + lane] : 0;
+        bool first = n > 0;
+        int32_t m = n;
+        for (int jj = 0; jj < G; ++jj) {
+          const int32_t rj = __shfl_sync(0xffffffffu, r, jj), nj = __shfl_sync(0xffffffffu, n, jj);
+          if (jj != lane && nj > 0 && rj == r) {
+            if (jj < lane) first = false;
+            m = nj > m ? nj : m;
           }
-          if (first) tiles += (m + kBlockM - 1) / kBlockM;
         }
-        sGroupOff[g] = tiles;
+        const int32_t tiles = __reduce_add_sync(0xffffffffu, (first ? (m + kBlockM - 1) / kBlockM : 0));
+        if (lane == 0) sGroupOff[g] = tiles;
       }
     }
     __syncthreads();
