@@ -368,9 +368,8 @@ __global__ void touch_kernel(const uint8_t* const* host_rows, const int32_t* seq
       // the page's first word inside the rows; 16-byte aligned, so the 4 bytes lie below end.
       // A volatile load: the value is unused, and a plain one could be dropped as dead code.
       const uint64_t addr = max(base, pg * (uint64_t)page);
-      uint32_t v;
+      [[maybe_unused]] uint32_t v;
       asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
-      (void)v;
     }
   }
 }
