@@ -57,6 +57,10 @@ def _load():
         lib.orc_hisparse_resolve.argtypes = [i32, i32, i32, i32, P, P, P, P, i32, P, P, i64, P, P,
                                              P, P, i64, P, P, ctypes.c_int]
         lib.orc_hisparse_resolve.restype = ctypes.c_int
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_kv_append.argtypes = [i32, i32, P, P, P, i32, P, P, P, i32, P, i64, P, P, i64]
+        lib.orc_kv_append.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -171,3 +175,31 @@ def hisparse_resolve(step: int, idx, seq_len, resident_start, block_table, host_
     if st:
         raise OracleError("resolve: idx not strictly ascending / out of range, or k > S")
     return out_rows, counters
+
+
+def e4m3_encode(x: float) -> int:
+    """OCP e4m3 code of a binary32 value (round to nearest even, saturating at +-448)."""
+    return int(_load().orc_e4m3_encode(float(np.float32(x))))
+
+
+def kv_append(latent_bits, rope_bits, index_key_bits, token_req, token_pos, block_table, kv_pool, k_cache,
+              k_scale, B: int) -> None:
+    """Quantises new tokens into ``kv_pool`` (uint8 [R, 656]) and ``k_cache`` / ``k_scale``
+    (uint8 [nblk, 64, Di], float32 [nblk, 64]) in place. ``*_bits`` are uint16 bf16 bit patterns
+    ([T, 512], [T, 64], [T, Di]); pass ``latent_bits=None`` or ``index_key_bits=None`` to skip that
+    part. Raises OracleError if a token's request, position or block is out of range."""
+    T = int(token_req.shape[0])
+    lat = None if latent_bits is None else _c(latent_bits, np.uint16)
+    rope = None if latent_bits is None else _c(rope_bits, np.uint16)
+    key = None if index_key_bits is None else _c(index_key_bits, np.uint16)
+    Di = 0 if key is None else int(key.shape[1])
+    for a, dt in ((kv_pool, np.uint8), (k_cache, np.uint8), (k_scale, np.float32)):
+        if a is not None and not (a.dtype == dt and a.flags.c_contiguous):
+            raise OracleError("kv_pool / k_cache / k_scale must be C-contiguous of their dtype (updated in place)")
+    bt = _c(block_table, np.int32)
+    st = _load().orc_kv_append(T, int(B), _p(lat), _p(rope), _p(key), Di, _p(_c(token_req, np.int32)),
+                               _p(_c(token_pos, np.int32)), _p(bt), bt.shape[1], _p(kv_pool),
+                               0 if kv_pool is None else kv_pool.shape[0], _p(k_cache), _p(k_scale),
+                               0 if k_cache is None else k_cache.shape[0])
+    if st:
+        raise OracleError("a token's request, position or block is out of range")

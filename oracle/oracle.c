@@ -495,3 +495,102 @@ int orc_hisparse_resolve(int32_t B, int32_t k, int32_t S, int32_t step, const in
   orc_parallel_for(B, threads, resolve_request, &c);
   return c.status;
 }
+
+/* ---------------------------------------------------------------- KV append ----------- */
+/*
+ * Quantise new tokens into the paged FP8 layouts the other operations read.
+ * [P1] 「数字がうまくいく理由」: a token's MLA KV is a 656-byte FP8 row (fp8_ds_mla format) and its
+ * indexer key is 128 FP8 values with a 4-byte scale. The row is read as
+ *   [512 x e4m3 latent codes][4 x fp32 scales, one per 128-dim group][64 x bf16 RoPE],
+ * the key as e4m3 codes [Di] plus one fp32 scale. The pages do not print the quantiser; the
+ * plain reading used here: per group (latent) or per key (indexer), in IEEE binary32,
+ *   scale = max(amax / 448, 2^-14),   code = e4m3_rn_satfinite(x / scale),
+ * with x the bf16 input value. These are integer decisions taken from binary32 arithmetic, so
+ * this function computes in binary32 (float), not in double: the definition is the binary32 one.
+ */
+
+/* OCP e4m3 encoding of a binary32 value: round to nearest, ties to an even mantissa; finite values
+ * beyond 448 (and infinities) saturate to +-448; NaN gives S.1111.111. */
+uint8_t orc_e4m3_encode(float x) {
+  if (isnan(x)) return signbit(x) ? 0xFF : 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9; 8 * 2^-9 is the smallest normal (code 0x08) */
+    const double q = nearbyint(ldexp(a, 9));
+    return sign | (uint8_t)q;
+  }
+  int e;
+  frexp(a, &e);                         /* a = f * 2^e, f in [0.5, 1): a in [2^(e-1), 2^e) */
+  const int E = e - 1;                  /* a in [2^E, 2^(E+1)) */
+  double q = nearbyint(ldexp(a, 3 - E));  /* 8 + mantissa, in [8, 16] */
+  int EE = E;
+  if (q >= 16.0) {
+    q = 8.0;
+    EE = E + 1;
+  }
+  const int code = ((EE + 7) << 3) | ((int)q - 8);
+  return sign | (uint8_t)(code > 0x7E ? 0x7E : code);
+}
+
+static float bf16_to_float(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+static float group_scale(const uint16_t* x, int n) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    const float v = fabsf(bf16_to_float(x[i]));
+    if (v > amax) amax = v;
+  }
+  const float s = amax / 448.0f;
+  const float floor_s = 6.103515625e-05f; /* 2^-14 */
+  return s > floor_s ? s : floor_s;
+}
+
+/*
+ * For each new token t (request token_req[t] < B, absolute position token_pos[t] >= 0): its row is
+ * bt[r][pos / 64] * 64 + pos % 64. latent [T,512], rope [T,64], index_key [T,Di] are bf16 bit
+ * patterns; any of latent (with rope) or index_key may be NULL (that part is not written).
+ * Returns 1 (nothing written for that token) when a token's request, position or block is out of
+ * range.
+ */
+int orc_kv_append(int32_t T, int32_t B, const uint16_t* latent, const uint16_t* rope, const uint16_t* index_key,
+                  int32_t Di, const int32_t* token_req, const int32_t* token_pos, const int32_t* block_table,
+                  int32_t bt_stride, uint8_t* kv_pool, int64_t R, uint8_t* k_cache, float* k_scale, int64_t nblk) {
+  int status = 0;
+  for (int32_t t = 0; t < T; ++t) {
+    const int32_t r = token_req[t], pos = token_pos[t];
+    if (r < 0 || r >= B || pos < 0 || pos / ORC_PAGE >= bt_stride) {
+      status = 1;
+      continue;
+    }
+    const int32_t blk = block_table[(int64_t)r * bt_stride + pos / ORC_PAGE];
+    const int64_t row = (int64_t)blk * ORC_PAGE + pos % ORC_PAGE;
+    if (blk < 0 || (latent && row >= R) || (index_key && blk >= nblk)) {
+      status = 1;
+      continue;
+    }
+    if (latent) {
+      uint8_t* dst = kv_pool + row * ORC_ROW;
+      for (int g = 0; g < ORC_DL / 128; ++g) {
+        const uint16_t* x = latent + (int64_t)t * ORC_DL + 128 * g;
+        const float s = group_scale(x, 128);
+        for (int c = 0; c < 128; ++c) dst[128 * g + c] = orc_e4m3_encode(bf16_to_float(x[c]) / s);
+        memcpy(dst + ORC_DL + 4 * g, &s, 4);
+      }
+      memcpy(dst + ORC_DL + 16, rope + (int64_t)t * ORC_DR, 2 * ORC_DR);
+    }
+    if (index_key) {
+      const uint16_t* x = index_key + (int64_t)t * Di;
+      const float s = group_scale(x, Di);
+      for (int c = 0; c < Di; ++c) k_cache[row * Di + c] = orc_e4m3_encode(bf16_to_float(x[c]) / s);
+      k_scale[row] = s;
+    }
+  }
+  return status;
+}
