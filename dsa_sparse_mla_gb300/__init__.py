@@ -15,7 +15,7 @@ import torch
 
 __all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
            "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_sparse_mla_fwd_static", "hs_hisparse_resolve",
-           "hs_hisparse_touch_host", "FLAGS"]
+           "hs_hisparse_touch_host", "hs_kv_append", "FLAGS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libhs.so")
@@ -80,8 +80,9 @@ def load():
         lib.hs_sparse_mla_fwd_static.argtypes = [ctypes.POINTER(_MlaArgs), _P]
         lib.hs_hisparse_resolve.argtypes = [ctypes.POINTER(_ResolveArgs), _P]
         lib.hs_hisparse_touch_host.argtypes = [_i32, _P, _P, _P, _P, _P]
+        lib.hs_kv_append.argtypes = [ctypes.POINTER(_AppendArgs), _P]
         for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
-                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve", "hs_hisparse_touch_host"):
+                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve", "hs_hisparse_touch_host", "hs_kv_append"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -226,3 +227,32 @@ def hs_hisparse_touch_host(host_rows, seq_len, resident_start, err_flag, stream=
         raise HSError(1, "host_rows, seq_len and resident_start must have the same length")
     _check(load().hs_hisparse_touch_host(B, _ptr(host_rows), _ptr(seq_len), _ptr(resident_start), _ptr(err_flag),
                                          _stream(stream)))
+
+
+class _AppendArgs(ctypes.Structure):
+    _fields_ = [("T", _i32), ("B", _i32), ("latent", _P), ("rope", _P), ("index_key", _P), ("Di", _i32),
+                ("token_req", _P), ("token_pos", _P), ("block_table", _P), ("bt_stride", _i32),
+                ("kv_pool", _P), ("R", _i64), ("k_cache", _P), ("k_scale", _P), ("nblk", _i64), ("err_flag", _P)]
+
+
+def hs_kv_append(token_req, token_pos, block_table, err_flag, latent=None, rope=None, kv_pool=None,
+                 index_key=None, k_cache=None, k_scale=None, stream=None):
+    """Quantise new tokens into the paged FP8 layouts (see include/hs.h). ``latent`` / ``rope`` are
+    bf16 [T, 512] / [T, 64] written into ``kv_pool`` (uint8 [R, 656]); ``index_key`` is bf16 [T, Di]
+    written into ``k_cache`` (uint8 [nblk, 64, Di]) and ``k_scale`` (float32 [nblk, 64])."""
+    _dev(token_req, "token_req", torch.int32), _dev(token_pos, "token_pos", torch.int32)
+    _dev(block_table, "block_table", torch.int32), _dev(err_flag, "err_flag", torch.int32)
+    a = _AppendArgs()
+    a.T, a.B = token_req.shape[0], block_table.shape[0]
+    if latent is not None:
+        _dev(latent, "latent", torch.bfloat16), _dev(rope, "rope", torch.bfloat16), _dev(kv_pool, "kv_pool", torch.uint8)
+        a.latent, a.rope, a.kv_pool, a.R = _ptr(latent), _ptr(rope), _ptr(kv_pool), kv_pool.shape[0]
+    if index_key is not None:
+        _dev(index_key, "index_key", torch.bfloat16), _dev(k_cache, "k_cache", torch.uint8)
+        _dev(k_scale, "k_scale", torch.float32)
+        a.index_key, a.Di, a.k_cache, a.k_scale, a.nblk = _ptr(index_key), index_key.shape[1], _ptr(k_cache), \
+            _ptr(k_scale), k_cache.shape[0]
+    a.token_req, a.token_pos, a.block_table, a.bt_stride = _ptr(token_req), _ptr(token_pos), _ptr(block_table), \
+        block_table.shape[1]
+    a.err_flag = _ptr(err_flag)
+    _check(load().hs_kv_append(ctypes.byref(a), _stream(stream)))

@@ -14,6 +14,7 @@ cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* kvlen, i
 cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const char** why);
 uint64_t mla_workspace_bytes(int32_t H, int sms);
 cudaError_t launch_resolve(const hs_resolve_args* a, cudaStream_t stream);
+cudaError_t launch_append(const hs_kv_append_args* a, int sms, cudaStream_t stream);
 cudaError_t launch_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,
                               const int32_t* resident_start, int64_t page, int32_t* err, cudaStream_t stream);
 }  // namespace hs
@@ -194,6 +195,31 @@ hs_status hs_hisparse_resolve(const hs_resolve_args* a, hs_stream_t stream) {
   hs_status st = check_device(nullptr);
   if (st != HS_OK) return st;
   return launched(hs::launch_resolve(a, (cudaStream_t)stream), "hs_hisparse_resolve", nullptr);
+}
+
+hs_status hs_kv_append(const hs_kv_append_args* a, hs_stream_t stream) {
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->T >= 0, "T must be >= 0");
+  REQUIRE(a->err_flag, "err_flag is NULL");
+  if (a->T == 0) return ok();
+  REQUIRE(a->B >= 1, "B must be >= 1");
+  REQUIRE(a->latent || a->index_key, "nothing to append: latent and index_key are both NULL");
+  REQUIRE(a->token_req && a->token_pos && a->block_table && a->bt_stride >= 1,
+          "token_req, token_pos and block_table are required (bt_stride >= 1)");
+  if (a->latent) {
+    REQUIRE(a->rope && a->kv_pool && a->R >= 1, "latent needs rope, kv_pool and R >= 1");
+    REQUIRE(aligned16(a->latent) && aligned16(a->rope) && aligned16(a->kv_pool),
+            "latent, rope and kv_pool must be 16-byte aligned");
+  }
+  if (a->index_key) {
+    REQUIRE(a->Di == 64 || a->Di == 128, "Di must be 64 or 128 (got %d)", a->Di);
+    REQUIRE(a->k_cache && a->k_scale && a->nblk >= 1, "index_key needs k_cache, k_scale and nblk >= 1");
+    REQUIRE(aligned16(a->index_key) && aligned16(a->k_cache), "index_key and k_cache must be 16-byte aligned");
+  }
+  int sms = 0;
+  hs_status st = check_device(&sms);
+  if (st != HS_OK) return st;
+  return launched(hs::launch_append(a, sms, (cudaStream_t)stream), "hs_kv_append", nullptr);
 }
 
 hs_status hs_hisparse_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,

@@ -76,7 +76,7 @@ typedef enum {
 #define HS_D_LATENT 512          /* latent (value) width */
 #define HS_D_ROPE 64             /* RoPE width */
 #define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
-#define HS_ABI_VERSION 3
+#define HS_ABI_VERSION 4
 
 int hs_abi_version(void);
 const char* hs_status_str(hs_status s);
@@ -310,6 +310,51 @@ hs_status hs_hisparse_resolve(const hs_resolve_args* a, hs_stream_t stream);
  * ---------------------------------------------------------------------------------------- */
 hs_status hs_hisparse_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,
                                  const int32_t* resident_start, int32_t* err_flag, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_kv_append — quantise new tokens into the paged FP8 layouts the other calls read.
+ *
+ * [P1] 「数字がうまくいく理由」: a token's MLA KV is a 656-byte FP8 row and its indexer key is 128
+ * FP8 values with a 4-byte scale. For each new token t of request token_req[t] at absolute
+ * position token_pos[t], row = block_table[r][pos / 64] * 64 + pos % 64 receives
+ *   kv_pool[row]  = [512 x e4m3 latent][4 x fp32 scales, one per 128-dim group][64 x bf16 RoPE]
+ *   k_cache[row]  = Di x e4m3,  k_scale[row] = fp32
+ * with, per latent group and per key, in IEEE binary32:
+ *   scale = max(amax / 448, 2^-14),  code = e4m3(x / scale) (nearest even, saturating at +-448).
+ * Inputs must be finite.
+ *
+ *   T, B            new tokens, requests (token_req[t] in [0, B))
+ *   latent, rope    bf16 [T, 512] and [T, 64] (16-byte aligned), or latent = NULL: no MLA rows
+ *   index_key       bf16 [T, Di] (16-byte aligned), Di in {64, 128}, or NULL: no indexer keys
+ *   token_req, token_pos   int32 [T]
+ *   block_table     int32 [B, bt_stride]
+ *   kv_pool, R      uint8 [R, 656] (16-byte aligned), needed with latent
+ *   k_cache, k_scale, nblk   uint8 [nblk, 64, Di] (16-byte aligned), fp32 [nblk, 64], needed with
+ *                   index_key
+ *   err_flag        a token with a request or position out of range sets HS_FLAG_BAD_INDEX, one
+ *                   whose block is negative or past the pool/cache sets HS_FLAG_BAD_BLOCK; such a
+ *                   token writes nothing. Two tokens mapping to one row race (caller error).
+ * Asynchronous on `stream`; allocates nothing.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t T, B;
+  const void* latent;
+  const void* rope;
+  const void* index_key;
+  int32_t Di;
+  const int32_t* token_req;
+  const int32_t* token_pos;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  uint8_t* kv_pool;
+  int64_t R;
+  uint8_t* k_cache;
+  float* k_scale;
+  int64_t nblk;
+  int32_t* err_flag;
+} hs_kv_append_args;
+
+hs_status hs_kv_append(const hs_kv_append_args* a, hs_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert hs.hs_abi_version() == 3
+    assert hs.hs_abi_version() == 4
     hs.load()
     for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                                  "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
@@ -60,6 +60,13 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1
     r.k, r.S = 8, 9000                                                # S too large
     assert L.hs_hisparse_resolve(ctypes.byref(r), None) == 1
+    ap = hs._AppendArgs()
+    ap.T, ap.B = 4, 1
+    ap.err_flag = 16
+    assert L.hs_kv_append(ctypes.byref(ap), None) == 1 and b"nothing to append" in L.hs_last_error()
+    ap.index_key, ap.Di = 16, 32
+    ap.token_req, ap.token_pos, ap.block_table, ap.bt_stride = 16, 16, 16, 1
+    assert L.hs_kv_append(ctypes.byref(ap), None) == 1 and b"Di must be" in L.hs_last_error()
     assert L.hs_hisparse_touch_host(-1, None, None, None, None, None) == 1
     assert L.hs_hisparse_touch_host(2, None, None, None, ctypes.c_void_p(16), None) == 1
     assert b"NULL" in L.hs_last_error()
