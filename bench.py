@@ -465,6 +465,45 @@ def run_long_prefill(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kv_append(args):
+    """FP8 KV append of N new tokens (512-d latent + 64-d RoPE + 128-d indexer key, bf16) spread over
+    64 requests of a paged pool with a random block table; median device time with an L2 flush
+    before each launch. Algorithmic bytes per token: reads 1024 + 128 + 256 (inputs) + 12
+    (request, position, block entry), writes 656 (row) + 128 (key) + 4 (key scale)."""
+    import torch
+    import dsa_sparse_mla_gb300 as hs
+    torch.cuda.set_device(0)
+    hs.load()
+    N, B = args.kv_append, 64
+    pages = (N + B * 64 - 1) // (B * 64)
+    nblk = B * pages
+    g = torch.Generator(device="cuda").manual_seed(0)
+    latent = torch.randn(N, 512, device="cuda", generator=g).to(torch.bfloat16)
+    rope = torch.randn(N, 64, device="cuda", generator=g).to(torch.bfloat16)
+    key = torch.randn(N, 128, device="cuda", generator=g).to(torch.bfloat16)
+    bt = torch.randperm(nblk, device="cuda", generator=g).view(B, pages).int()
+    ar = torch.arange(N, device="cuda", dtype=torch.int32)
+    req, pos = (ar % B).contiguous(), (ar // B).contiguous()
+    kv = torch.empty((nblk * 64, 656), dtype=torch.uint8, device="cuda")
+    kc = torch.empty((nblk, 64, 128), dtype=torch.uint8, device="cuda")
+    ks = torch.empty((nblk, 64), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fn = lambda: hs.hs_kv_append(req, pos, bt, err, latent=latent, rope=rope, kv_pool=kv, index_key=key, k_cache=kc,
+                                 k_scale=ks)
+    t = _timed(fn, flush, max(args.reps, 5))
+    per_tok = 1024 + 128 + 256 + 12 + 656 + 128 + 4
+    gbs = N * per_tok / (t * 1e6)
+    peaks, kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    line = {"metric": "FP8 KV append (quantise + paged write) tokens/s", "tokens": N, "requests": B,
+            "value": round(N / (t * 1e-3), 1), "unit": "tokens/s", "ms": round(t, 4),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                         "bytes_per_token": per_tok, "peak_source": "%s (MEASURED_PEAKS.json)" % kind},
+            "device_flag": hs.hs_check_flag(err), "l2": "256 MB write before each timed launch", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+
+
 def run_hisparse(args):
     """HiSparse mixed-residency decode: 32 requests, contexts U{262144..1048576}, the last 4,096
     tokens resident, older rows in pinned host memory, 4,096 hot slots per request; 50 steps of
@@ -575,10 +614,13 @@ def main(argv=None):
     ap.add_argument("--chunk-stride", type=int, default=1, help="--config 4: time every n-th chunk")
     ap.add_argument("--reps", type=int, default=5, help="--config 4: timed launches per kernel and chunk")
     ap.add_argument("--hisparse-steps", type=int, default=50, help="--config 5: decode steps")
+    ap.add_argument("--kv-append", type=int, default=0, help="time hs_kv_append on this many new tokens instead")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.kv_append > 0:
+        run_kv_append(args)
     elif args.config == 4:
         run_long_prefill(args)
     elif args.config == 5:

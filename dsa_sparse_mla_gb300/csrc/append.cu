@@ -10,13 +10,15 @@
 //
 // One warp per token: lane l quantises latent values 16 l .. 16 l + 15 (a 128-dim group is 8 lanes,
 // its amax three shuffles) and writes them as one 16-byte store; lanes 0-7 copy the RoPE part; the
-// key is spread over the whole warp. Memory-bound: ~2.2 KB of traffic per token.
+// key is spread over the whole warp. Warps stride over the tokens with the next token's inputs
+// loaded while the current one is quantised. Memory-bound: 2,208 bytes of traffic per token.
 #include "common.cuh"
 
 namespace hs {
 namespace append {
 
 constexpr int kWarps = 8;
+constexpr int kCtasPerSm = 4;  // registers for the prefetched token: 64 a thread
 constexpr float kScaleFloor = 6.103515625e-05f;  // 2^-14
 
 struct Params {
@@ -49,71 +51,98 @@ __device__ __forceinline__ float quant_scale(float amax) {
   return fmaxf(__fdiv_rn(amax, 448.0f), kScaleFloor);
 }
 
-__global__ void __launch_bounds__(32 * kWarps) append_kernel(const Params p) {
+// One token's inputs as a lane holds them: latent values 16 l .. 16 l + 15, RoPE piece l (lanes
+// 0-7), key values (Di / 32 per lane), and the token's request and position.
+struct TokenIn {
+  uint4 la, lb, rp;
+  uint2 k;
+  int32_t r, pos;
+};
+
+__device__ __forceinline__ TokenIn load_token(const Params& p, int64_t t, int lane) {
+  TokenIn in;
+  in.r = p.token_req[t];
+  in.pos = p.token_pos[t];
+  if (p.latent) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.latent + t * HS_D_LATENT) + 2 * lane;
+    in.la = src[0];
+    in.lb = src[1];
+    if (lane < 8) in.rp = reinterpret_cast<const uint4*>(p.rope + t * HS_D_ROPE)[lane];
+  }
+  if (p.key) {
+    if (p.Di == 128) {
+      in.k = reinterpret_cast<const uint2*>(p.key + t * 128)[lane];
+    } else {
+      in.k.x = reinterpret_cast<const uint32_t*>(p.key + t * 64)[lane];
+      in.k.y = 0u;
+    }
+  }
+  return in;
+}
+
+__global__ void __launch_bounds__(32 * kWarps, kCtasPerSm) append_kernel(const Params p) {
   const int lane = threadIdx.x & 31;
-  for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < p.T; t += (int64_t)gridDim.x * kWarps) {
-    const int32_t r = p.token_req[t], pos = p.token_pos[t];
-    if (r < 0 || r >= p.B || pos < 0 || pos / 64 >= p.bt_stride) {
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= p.T) return;
+  TokenIn cur = load_token(p, t, lane);
+  for (; t < p.T; t += stride) {
+    // the next token's loads are in flight while this one is quantised and stored
+    TokenIn nxt;
+    if (t + stride < p.T) nxt = load_token(p, t + stride, lane);
+    const int32_t r = cur.r, pos = cur.pos;
+    bool ok = !(r < 0 || r >= p.B || pos < 0 || pos / 64 >= p.bt_stride);
+    if (!ok) {
       if (lane == 0) flag_error(p.err, HS_FLAG_BAD_INDEX);
-      continue;
-    }
-    const int32_t blk = p.bt[(int64_t)r * p.bt_stride + pos / 64];
-    const int64_t row = (int64_t)blk * 64 + (pos & 63);
-    if (blk < 0 || (p.latent && row >= p.R) || (p.key && blk >= p.nblk)) {
-      if (lane == 0) flag_error(p.err, HS_FLAG_BAD_BLOCK);
-      continue;
-    }
-    if (p.latent) {
-      const uint4* src = reinterpret_cast<const uint4*>(p.latent + t * HS_D_LATENT) + 2 * lane;
-      const uint4 a = src[0], b = src[1];
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      float x[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        x[2 * i] = bf16_lo(w[i]);
-        x[2 * i + 1] = bf16_hi(w[i]);
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float s = quant_scale(amax);
-      uint32_t c[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        c[i] = e4m3x2(__fdiv_rn(x[4 * i], s), __fdiv_rn(x[4 * i + 1], s)) |
-               (e4m3x2(__fdiv_rn(x[4 * i + 2], s), __fdiv_rn(x[4 * i + 3], s)) << 16);
-      uint8_t* dst = p.kv + row * HS_KV_ROW_BYTES;
-      *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(c[0], c[1], c[2], c[3]);
-      if ((lane & 7) == 0) *reinterpret_cast<float*>(dst + HS_D_LATENT + 4 * (lane >> 3)) = s;
-      if (lane < 8)
-        reinterpret_cast<uint4*>(dst + HS_D_LATENT + 16)[lane] =
-            reinterpret_cast<const uint4*>(p.rope + t * HS_D_ROPE)[lane];
-    }
-    if (p.key) {
-      // Di / 32 values per lane (4 or 2)
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (p.Di == 128) {
-        const uint2 v = reinterpret_cast<const uint2*>(p.key + t * 128)[lane];
-        x[0] = bf16_lo(v.x), x[1] = bf16_hi(v.x), x[2] = bf16_lo(v.y), x[3] = bf16_hi(v.y);
+    } else {
+      const int32_t blk = p.bt[(int64_t)r * p.bt_stride + pos / 64];
+      const int64_t row = (int64_t)blk * 64 + (pos & 63);
+      if (blk < 0 || (p.latent && row >= p.R) || (p.key && blk >= p.nblk)) {
+        if (lane == 0) flag_error(p.err, HS_FLAG_BAD_BLOCK);
       } else {
-        const uint32_t v = reinterpret_cast<const uint32_t*>(p.key + t * 64)[lane];
-        x[0] = bf16_lo(v), x[1] = bf16_hi(v);
-      }
-      float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+        if (p.latent) {
+          const uint32_t w[8] = {cur.la.x, cur.la.y, cur.la.z, cur.la.w, cur.lb.x, cur.lb.y, cur.lb.z, cur.lb.w};
+          float x[16];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const float s = quant_scale(amax);
-      const uint32_t lo = e4m3x2(__fdiv_rn(x[0], s), __fdiv_rn(x[1], s));
-      if (p.Di == 128) {
-        const uint32_t hi = e4m3x2(__fdiv_rn(x[2], s), __fdiv_rn(x[3], s));
-        reinterpret_cast<uint32_t*>(p.k_cache + row * 128)[lane] = lo | (hi << 16);
-      } else {
-        reinterpret_cast<uint16_t*>(p.k_cache + row * 64)[lane] = (uint16_t)lo;
+          for (int i = 0; i < 8; ++i) {
+            x[2 * i] = bf16_lo(w[i]);
+            x[2 * i + 1] = bf16_hi(w[i]);
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const float s = quant_scale(amax);
+          uint32_t c[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            c[i] = e4m3x2(__fdiv_rn(x[4 * i], s), __fdiv_rn(x[4 * i + 1], s)) |
+                   (e4m3x2(__fdiv_rn(x[4 * i + 2], s), __fdiv_rn(x[4 * i + 3], s)) << 16);
+          uint8_t* dst = p.kv + row * HS_KV_ROW_BYTES;
+          *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(c[0], c[1], c[2], c[3]);
+          if ((lane & 7) == 0) *reinterpret_cast<float*>(dst + HS_D_LATENT + 4 * (lane >> 3)) = s;
+          if (lane < 8) reinterpret_cast<uint4*>(dst + HS_D_LATENT + 16)[lane] = cur.rp;
+        }
+        if (p.key) {
+          const float x0 = bf16_lo(cur.k.x), x1 = bf16_hi(cur.k.x);
+          const float x2 = p.Di == 128 ? bf16_lo(cur.k.y) : 0.f, x3 = p.Di == 128 ? bf16_hi(cur.k.y) : 0.f;
+          float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const float s = quant_scale(amax);
+          const uint32_t lo = e4m3x2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+          if (p.Di == 128) {
+            const uint32_t hi = e4m3x2(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
+            reinterpret_cast<uint32_t*>(p.k_cache + row * 128)[lane] = lo | (hi << 16);
+          } else {
+            reinterpret_cast<uint16_t*>(p.k_cache + row * 64)[lane] = (uint16_t)lo;
+          }
+          if (lane == 0) p.k_scale[row] = s;
+        }
       }
-      if (lane == 0) p.k_scale[row] = s;
     }
+    cur = nxt;
   }
 }
 
@@ -140,7 +169,8 @@ cudaError_t launch_append(const hs_kv_append_args* a, int sms, cudaStream_t stre
   p.err = a->err_flag;
   if (a->T == 0) return cudaSuccess;
   int64_t blocks = ((int64_t)a->T + kWarps - 1) / kWarps;
-  if (blocks > 8LL * sms) blocks = 8LL * sms;  // grid-stride beyond eight CTAs per SM
+  // two waves of resident CTAs (measured faster than one); warps stride over the rest
+  if (blocks > 2LL * kCtasPerSm * sms) blocks = 2LL * kCtasPerSm * sms;
   append_kernel<<<(unsigned)blocks, 32 * kWarps, 0, stream>>>(p);
   return cudaGetLastError();
 }
