@@ -137,7 +137,7 @@ class ClockSampler:
 # ------------------------------------------------------------------------ traffic record -----
 
 def kernel_source_digest(kernel: str) -> str:
-    src = {"indexer": "indexer.cu", "topk": "topk.cu", "mla": "mla.cu", "resolve": "resolve.cu"}[kernel]
+    src = {"indexer": "indexer.cu", "topk": "topk.cu", "mla": "mla.cu", "resolve": "resolve.cu", "append": "append.cu"}[kernel]
     h = hashlib.sha256()
     for f in (src, "common.cuh"):
         with open(os.path.join(ROOT, "dsa_sparse_mla_gb300", "csrc", f), "rb") as fh:
@@ -499,7 +499,8 @@ def run_kv_append(args):
     line = {"metric": "FP8 KV append (quantise + paged write) tokens/s", "tokens": N, "requests": B,
             "value": round(N / (t * 1e-3), 1), "unit": "tokens/s", "ms": round(t, 4),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-                         "bytes_per_token": per_tok, "peak_source": "%s (MEASURED_PEAKS.json)" % kind},
+                         "bytes_per_token": per_tok, "peak_source": "%s (MEASURED_PEAKS.json)" % kind,
+                         "traffic": recorded_traffic("append", "kv-append-%d" % N)},
             "device_flag": hs.hs_check_flag(err), "l2": "256 MB write before each timed launch", "data": "synthetic"}
     print(json.dumps(line), flush=True)
 
