@@ -61,6 +61,8 @@ def _load():
         lib.orc_e4m3_encode.restype = ctypes.c_uint8
         lib.orc_kv_append.argtypes = [i32, i32, P, P, P, i32, P, P, P, i32, P, i64, P, P, i64]
         lib.orc_kv_append.restype = ctypes.c_int
+        lib.orc_kv_offload.argtypes = [i32, i32, i32, P, i64, P, P, P, P, P, i32, P]
+        lib.orc_kv_offload.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -197,9 +199,29 @@ def kv_append(latent_bits, rope_bits, index_key_bits, token_req, token_pos, bloc
         if a is not None and not (a.dtype == dt and a.flags.c_contiguous):
             raise OracleError("kv_pool / k_cache / k_scale must be C-contiguous of their dtype (updated in place)")
     bt = _c(block_table, np.int32)
-    st = _load().orc_kv_append(T, int(B), _p(lat), _p(rope), _p(key), Di, _p(_c(token_req, np.int32)),
-                               _p(_c(token_pos, np.int32)), _p(bt), bt.shape[1], _p(kv_pool),
+    treq, tpos = _c(token_req, np.int32), _c(token_pos, np.int32)  # kept alive across the call
+    st = _load().orc_kv_append(T, int(B), _p(lat), _p(rope), _p(key), Di, _p(treq), _p(tpos), _p(bt), bt.shape[1],
+                               _p(kv_pool),
                                0 if kv_pool is None else kv_pool.shape[0], _p(k_cache), _p(k_scale),
                                0 if k_cache is None else k_cache.shape[0])
     if st:
         raise OracleError("a token's request, position or block is out of range")
+
+
+def kv_offload(pools, host_rows, layer, req, page, block_table, seq_len) -> None:
+    """Copies complete pages from the per-layer pools (uint8 [R, 656] each) into the per-(layer,
+    request) host rows (uint8 [seq_len_r, 656]; list indexed layer * B + r), in place. Raises
+    OracleError if an entry is out of range."""
+    L, B = len(pools), int(np.asarray(block_table).shape[0])
+    R = int(pools[0].shape[0])
+    for a in list(pools) + list(host_rows):
+        if not (a.dtype == np.uint8 and a.flags.c_contiguous):
+            raise OracleError("pools and host rows must be C-contiguous uint8")
+    pp = (ctypes.c_void_p * L)(*[a.ctypes.data for a in pools])
+    hp = (ctypes.c_void_p * len(host_rows))(*[a.ctypes.data for a in host_rows])
+    bt = _c(block_table, np.int32)
+    lay, rq, pg, sl = _c(layer, np.int32), _c(req, np.int32), _c(page, np.int32), _c(seq_len, np.int32)  # kept alive
+    st = _load().orc_kv_offload(int(lay.shape[0]), L, B, ctypes.addressof(pp), R, ctypes.addressof(hp), _p(lay), _p(rq),
+                                _p(pg), _p(bt), bt.shape[1], _p(sl))
+    if st:
+        raise OracleError("an offload entry is out of range")

@@ -594,3 +594,34 @@ int orc_kv_append(int32_t T, int32_t B, const uint16_t* latent, const uint16_t* 
   }
   return status;
 }
+
+/* ---------------------------------------------------------------- KV offload ---------- */
+/*
+ * HiSparse write side: copy complete KV pages from the device pools to the host tier.
+ * [P3] 「主要なアーキテクチャ的詳細」: completed prefix pages are copied to host memory ahead of
+ * pressure, while the GPU still serves them, and all sparse-MLA layers are copied in one batch
+ * after the forward pass. Entry i copies page page[i] (tokens 64 p .. 64 p + 63) of request req[i]
+ * in layer layer[i]: the 64 rows of pool block block_table[r][p] of that layer's pool to rows
+ * 64 p .. 64 p + 63 of host_rows[layer * B + r]. A page must be complete: 64 (p + 1) <= seq_len[r].
+ * Returns 1 (that entry copies nothing) for an entry out of range.
+ */
+int orc_kv_offload(int32_t n, int32_t L, int32_t B, const uint8_t* const* pools, int64_t R,
+                   uint8_t* const* host_rows, const int32_t* layer, const int32_t* req, const int32_t* page,
+                   const int32_t* block_table, int32_t bt_stride, const int32_t* seq_len) {
+  int status = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t l = layer[i], r = req[i], p = page[i];
+    if (l < 0 || l >= L || r < 0 || r >= B || p < 0 || p >= bt_stride || (int64_t)ORC_PAGE * (p + 1) > seq_len[r]) {
+      status = 1;
+      continue;
+    }
+    const int32_t blk = block_table[(int64_t)r * bt_stride + p];
+    if (blk < 0 || (int64_t)(blk + 1) * ORC_PAGE > R) {
+      status = 1;
+      continue;
+    }
+    memcpy(host_rows[(int64_t)l * B + r] + (int64_t)p * ORC_PAGE * ORC_ROW, pools[l] + (int64_t)blk * ORC_PAGE * ORC_ROW,
+           (size_t)ORC_PAGE * ORC_ROW);
+  }
+  return status;
+}
