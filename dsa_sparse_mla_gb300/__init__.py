@@ -15,7 +15,7 @@ import torch
 
 __all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
            "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_sparse_mla_fwd_static", "hs_hisparse_resolve",
-           "hs_hisparse_touch_host", "hs_kv_append", "FLAGS"]
+           "hs_hisparse_touch_host", "hs_kv_append", "hs_kv_offload", "FLAGS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libhs.so")
@@ -81,8 +81,9 @@ def load():
         lib.hs_hisparse_resolve.argtypes = [ctypes.POINTER(_ResolveArgs), _P]
         lib.hs_hisparse_touch_host.argtypes = [_i32, _P, _P, _P, _P, _P]
         lib.hs_kv_append.argtypes = [ctypes.POINTER(_AppendArgs), _P]
+        lib.hs_kv_offload.argtypes = [ctypes.POINTER(_OffloadArgs), _P]
         for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
-                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve", "hs_hisparse_touch_host", "hs_kv_append"):
+                  "hs_sparse_mla_fwd_static", "hs_hisparse_resolve", "hs_hisparse_touch_host", "hs_kv_append", "hs_kv_offload"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -256,3 +257,26 @@ def hs_kv_append(token_req, token_pos, block_table, err_flag, latent=None, rope=
         block_table.shape[1]
     a.err_flag = _ptr(err_flag)
     _check(load().hs_kv_append(ctypes.byref(a), _stream(stream)))
+
+
+class _OffloadArgs(ctypes.Structure):
+    _fields_ = [("n", _i32), ("L", _i32), ("B", _i32), ("pools", _P), ("R", _i64), ("host_rows", _P), ("layer", _P),
+                ("req", _P), ("page", _P), ("block_table", _P), ("bt_stride", _i32), ("seq_len", _P), ("err_flag", _P)]
+
+
+def hs_kv_offload(pools, host_rows, layer, req, page, block_table, seq_len, err_flag, R: int, stream=None):
+    """Copy complete KV pages to the host tier (see include/hs.h). ``pools`` is an int64 CUDA tensor
+    [L] of device pointers to each layer's pool (uint8 [R, 656]); ``host_rows`` an int64 CUDA tensor
+    [L * B] of device-accessible pointers to pinned host rows, indexed layer * B + request."""
+    for t, nm, dt in ((pools, "pools", torch.int64), (host_rows, "host_rows", torch.int64), (layer, "layer", torch.int32),
+                      (req, "req", torch.int32), (page, "page", torch.int32), (block_table, "block_table", torch.int32),
+                      (seq_len, "seq_len", torch.int32), (err_flag, "err_flag", torch.int32)):
+        _dev(t, nm, dt)
+    a = _OffloadArgs()
+    a.n, a.L, a.B = layer.shape[0], pools.shape[0], block_table.shape[0]
+    if host_rows.shape[0] != a.L * a.B:
+        raise HSError(1, "host_rows must hold L * B pointers")
+    a.pools, a.R, a.host_rows = _ptr(pools), int(R), _ptr(host_rows)
+    a.layer, a.req, a.page = _ptr(layer), _ptr(req), _ptr(page)
+    a.block_table, a.bt_stride, a.seq_len, a.err_flag = _ptr(block_table), block_table.shape[1], _ptr(seq_len), _ptr(err_flag)
+    _check(load().hs_kv_offload(ctypes.byref(a), _stream(stream)))

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libhs.so")
-SOURCES = ["hs_api.cu", "indexer.cu", "topk.cu", "mla.cu", "mla_static.cu", "resolve.cu", "append.cu"]
+SOURCES = ["hs_api.cu", "indexer.cu", "topk.cu", "mla.cu", "mla_static.cu", "resolve.cu", "append.cu", "offload.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

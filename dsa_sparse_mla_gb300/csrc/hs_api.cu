@@ -15,6 +15,7 @@ cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const
 uint64_t mla_workspace_bytes(int32_t H, int sms);
 cudaError_t launch_resolve(const hs_resolve_args* a, cudaStream_t stream);
 cudaError_t launch_append(const hs_kv_append_args* a, int sms, cudaStream_t stream);
+cudaError_t launch_offload(const hs_kv_offload_args* a, int sms, cudaStream_t stream);
 cudaError_t launch_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,
                               const int32_t* resident_start, int64_t page, int32_t* err, cudaStream_t stream);
 }  // namespace hs
@@ -220,6 +221,21 @@ hs_status hs_kv_append(const hs_kv_append_args* a, hs_stream_t stream) {
   hs_status st = check_device(&sms);
   if (st != HS_OK) return st;
   return launched(hs::launch_append(a, sms, (cudaStream_t)stream), "hs_kv_append", nullptr);
+}
+
+hs_status hs_kv_offload(const hs_kv_offload_args* a, hs_stream_t stream) {
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->n >= 0, "n must be >= 0");
+  REQUIRE(a->err_flag, "err_flag is NULL");
+  if (a->n == 0) return ok();
+  REQUIRE(a->L >= 1 && a->B >= 1, "L and B must be >= 1");
+  REQUIRE(a->pools && a->host_rows && a->layer && a->req && a->page && a->block_table && a->seq_len,
+          "a required pointer is NULL");
+  REQUIRE(a->bt_stride >= 1 && a->R >= 64, "bt_stride must be >= 1 and R >= 64");
+  int sms = 0;
+  hs_status st = check_device(&sms);
+  if (st != HS_OK) return st;
+  return launched(hs::launch_offload(a, sms, (cudaStream_t)stream), "hs_kv_offload", nullptr);
 }
 
 hs_status hs_hisparse_touch_host(int32_t B, const uint8_t* const* host_rows, const int32_t* seq_len,

@@ -76,7 +76,7 @@ typedef enum {
 #define HS_D_LATENT 512          /* latent (value) width */
 #define HS_D_ROPE 64             /* RoPE width */
 #define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
-#define HS_ABI_VERSION 4
+#define HS_ABI_VERSION 5
 
 int hs_abi_version(void);
 const char* hs_status_str(hs_status s);
@@ -355,6 +355,44 @@ typedef struct {
 } hs_kv_append_args;
 
 hs_status hs_kv_append(const hs_kv_append_args* a, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_kv_offload — HiSparse write side: copy complete KV pages to the host tier.
+ *
+ * [P3] 「主要なアーキテクチャ的詳細」: completed prefix pages are copied to host memory ahead of
+ * memory pressure, while the GPU still serves them, and after the forward pass all sparse-MLA
+ * layers are copied in one launch ordered on the model's stream. Entry i copies page p = page[i]
+ * (tokens 64 p .. 64 p + 63) of request r = req[i] in layer l = layer[i]: the 64 rows of block
+ * block_table[r][p] of pools[l] go to rows 64 p .. 64 p + 63 of host_rows[l * B + r]. Block ids
+ * are shared by all layers (one block table).
+ *
+ *   n, L, B         entries, layers, requests
+ *   pools           device array of L device pointers, each to uint8 [R, 656] (16-byte aligned)
+ *   host_rows       device array of L * B device-accessible pointers, each to pinned uint8
+ *                   [seq_len[r], 656] (16-byte aligned)
+ *   layer, req, page   int32 [n]
+ *   block_table     int32 [B, bt_stride];  seq_len int32 [B]
+ *   err_flag        an entry out of range, or a page not complete (64 (p + 1) > seq_len[r]), or a
+ *                   misaligned pointer sets HS_FLAG_BAD_INDEX; a negative block or one past R sets
+ *                   HS_FLAG_BAD_BLOCK; such an entry copies nothing.
+ * Asynchronous on `stream`; allocates nothing. Entries writing the same host rows race (caller
+ * error).
+ * ---------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t n, L, B;
+  const uint8_t* const* pools;
+  int64_t R;
+  uint8_t* const* host_rows;
+  const int32_t* layer;
+  const int32_t* req;
+  const int32_t* page;
+  const int32_t* block_table;
+  int32_t bt_stride;
+  const int32_t* seq_len;
+  int32_t* err_flag;
+} hs_kv_offload_args;
+
+hs_status hs_kv_offload(const hs_kv_offload_args* a, hs_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert hs.hs_abi_version() == 4
+    assert hs.hs_abi_version() == 5
     hs.load()
     for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                                  "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
@@ -67,6 +67,9 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     ap.index_key, ap.Di = 16, 32
     ap.token_req, ap.token_pos, ap.block_table, ap.bt_stride = 16, 16, 16, 1
     assert L.hs_kv_append(ctypes.byref(ap), None) == 1 and b"Di must be" in L.hs_last_error()
+    oa = hs._OffloadArgs()
+    oa.n, oa.L, oa.B, oa.err_flag = 3, 1, 1, 16
+    assert L.hs_kv_offload(ctypes.byref(oa), None) == 1 and b"NULL" in L.hs_last_error()
     assert L.hs_hisparse_touch_host(-1, None, None, None, None, None) == 1
     assert L.hs_hisparse_touch_host(2, None, None, None, ctypes.c_void_p(16), None) == 1
     assert b"NULL" in L.hs_last_error()
