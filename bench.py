@@ -505,6 +505,44 @@ def run_kv_append(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kv_offload(args):
+    """HiSparse write side: N complete pages (64 rows x 656 B) spread over 8 layers x 32 requests,
+    copied from the device pools into pinned host rows by hs_kv_offload; median device time with an
+    L2 flush before each launch. For context, the copy engine's rate on one contiguous
+    device-to-host copy of the same bytes is measured in the same run."""
+    import torch
+    import dsa_sparse_mla_gb300 as hs
+    from dsa_sparse_mla_gb300.pipeline import pinned_uint8
+    torch.cuda.set_device(0)
+    hs.load()
+    L, B = 8, 32
+    pages = max(1, (args.kv_offload + L * B - 1) // (L * B))
+    n = L * B * pages
+    g = torch.Generator(device="cuda").manual_seed(0)
+    nblk = B * pages
+    pools = [torch.randint(0, 256, (nblk * 64, 656), dtype=torch.uint8, device="cuda", generator=g) for _ in range(L)]
+    bt = torch.randperm(nblk, device="cuda", generator=g).view(B, pages).int()
+    hosts = [pinned_uint8(pages * 64 * 656) for _ in range(L * B)]
+    ar = torch.arange(n, device="cuda", dtype=torch.int32)
+    layer, req, page = (ar // (B * pages)).contiguous(), ((ar // pages) % B).contiguous(), (ar % pages).contiguous()
+    seq = torch.full((B,), pages * 64, dtype=torch.int32, device="cuda")
+    pp = torch.tensor([p.data_ptr() for p in pools], dtype=torch.int64, device="cuda")
+    hp = torch.tensor([h.ctypes.data for h in hosts], dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fn = lambda: hs.hs_kv_offload(pp, hp, layer, req, page, bt, seq, err, R=nblk * 64)
+    t = _timed(fn, flush, max(args.reps, 5))
+    nbytes = n * 64 * 656
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    t_ce = _timed(lambda: host.copy_(dev, non_blocking=True), flush, 5)
+    line = {"metric": "KV offload (device pages -> pinned host) GB/s", "pages": n, "layers": L, "requests": B,
+            "bytes": nbytes, "ms": round(t, 4), "value": round(nbytes / (t * 1e6), 1), "unit": "GB/s",
+            "copy_engine_gbs": round(nbytes / (t_ce * 1e6), 1), "frac_of_copy_engine": round(t_ce / t, 3),
+            "device_flag": hs.hs_check_flag(err), "l2": "256 MB write before each timed launch", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+
+
 def run_hisparse(args):
     """HiSparse mixed-residency decode: 32 requests, contexts U{262144..1048576}, the last 4,096
     tokens resident, older rows in pinned host memory, 4,096 hot slots per request; 50 steps of
@@ -616,12 +654,15 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=5, help="--config 4: timed launches per kernel and chunk")
     ap.add_argument("--hisparse-steps", type=int, default=50, help="--config 5: decode steps")
     ap.add_argument("--kv-append", type=int, default=0, help="time hs_kv_append on this many new tokens instead")
+    ap.add_argument("--kv-offload", type=int, default=0, help="time hs_kv_offload on about this many pages instead")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
     elif args.kv_append > 0:
         run_kv_append(args)
+    elif args.kv_offload > 0:
+        run_kv_offload(args)
     elif args.config == 4:
         run_long_prefill(args)
     elif args.config == 5:
