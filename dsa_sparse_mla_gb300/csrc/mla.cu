@@ -28,8 +28,14 @@
 //               as fp16 into the stage's RoPE block, which QK no longer needs, so P is double
 //               buffered with the stages. O^T lives in TMEM and is rescaled only
 //               when a head's running max grows by more than 2^8 (lazy rescaling); the final pass
-//               divides by the row sum and writes bf16.
+//               divides by the row sum and writes bf16 straight from TMEM (neighbouring lanes swap
+//               values so that each stores two adjacent dims of one head).
 // TMEM: columns 0-127 hold two S buffers (64-row layout), 128-383 hold O^T.
+//
+// Work split (launch_mla): one CTA per query when the queries fill their waves; otherwise, given a
+// workspace, one persistent CTA per SM takes an equal share of all (query, 64-row tile) units, a
+// query split between CTAs leaves a normalised partial and its LSE per CTA, and mla_merge_kernel
+// combines them (split-KV decode: DCP's log-sum-exp merge on one GPU).
 #include "common.cuh"
 
 namespace hs {
