@@ -9,6 +9,15 @@
  *   hs_hisparse_resolve serve each selected token from resident KV, the hot buffer (LRU),
  *                       or a copy from pinned host memory into an LRU slot
  *
+ * and around them:
+ *
+ *   hs_sparse_mla_workspace_size, hs_sparse_mla_fwd_static
+ *                       the MLA's optional split-work scratch (caller-provided, or a fixed array
+ *                       inside the library)
+ *   hs_hisparse_touch_host  map the host tier for the GPU once, before the first resolve
+ *   hs_kv_append        quantise new tokens into the paged FP8 rows and indexer keys
+ *   hs_kv_offload       copy complete KV pages of every layer to the pinned host tier
+ *
  * Sources (web pages describing GLM-5.x serving with DSA in vLLM):
  *   [P1] "vLLM v0.32.0 GLM-5.3 サービング: 16基のH200上でのPCP、DCP、およびハイブリッドHiSparse"
  *   [P2] "Optimizaciones de GLM-5.3, Parte 2: PCP, DCP e Hybrid HiSparse en 16 H200"
@@ -17,7 +26,8 @@
  *
  * Conventions shared by every call
  *  - All buffers are caller-owned device memory unless stated; the library allocates nothing
- *    and keeps no state between calls (hs_last_error's thread-local string aside).
+ *    and keeps no state between calls (hs_last_error's thread-local string aside; the fixed
+ *    scratch array of hs_sparse_mla_fwd_static is the one stated exception).
  *  - Every call only enqueues work on `stream` (NULL = legacy default stream); none waits on
  *    the host for the GPU.
  *  - Arguments are checked on the host first. A bad argument returns HS_ERR_INVALID and
