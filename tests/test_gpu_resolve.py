@@ -83,6 +83,12 @@ def test_replay_matches_oracle(B, k, S, n, res, steps, overlap):
     _replay(B, k, S, n, res, steps, overlap, seed=B * 7 + k)
 
 
+def test_replay_in_the_benchmark_launch_shape():
+    """32 requests, k = 2048, S = 4096 (one CTA per request, 4096-slot sort, as the mixed-residency
+    benchmark launches it); shorter contexts than the benchmark's so the oracle replays every step."""
+    _replay(32, 2048, 4096, 20000, 4096, 3, 0.8, seed=32)
+
+
 def test_replay_wide_stamp_spread():
     """Step numbers far apart (spreads of up to 2**30 between stamps): the victim order then needs
     every 4-bit digit of the stamp, not just the lowest ones."""
