@@ -46,7 +46,7 @@ def _worker(rank, world, port, out):
 
 def test_two_gloo_ranks():
     world = 2
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     out = manager.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0][0] == out[1][0] == 2.5               # max over ranks of 1.5, 2.5
