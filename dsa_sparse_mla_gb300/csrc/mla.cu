@@ -6,7 +6,7 @@
 // dims. Per query token t, head h, over the valid entries i of idx[t, :]:
 //   logit_i = scale * <q[t,h,:], [latent_i, rope_i]>,  out = softmax(logit) . latent,  lse = ln sum exp.
 //
-// One CTA per query token (448 threads):
+// One CTA per query token (416 threads):
 //   warps 0-7   gather 64 rows per tile (warp w owns rows 8w..8w+7; one 16-byte load per lane
 //               brings one 64-dim block of all 8 rows), dequantise latent = e4m3 * group scale to
 //               fp16 (exact e4m3 -> fp16 conversion, one rounding for the scale) and write it, with
@@ -14,22 +14,24 @@
 //               (2 stages). Blocks are published in pairs as soon as they are written (a barrier
 //               per block), so QK starts on the first blocks while later ones are still being
 //               written; PV releases the stage pair by pair (one barrier per 128-dim M-tile),
-//               so the next tile's first blocks are written while PV still reads the last ones;
+//               so the next tile's first blocks are written while PV still reads the last ones.
+//               Producers load and dequantise the next tile into registers while they wait for a
+//               free stage, so global-memory latency is off the MMA chain;
 //   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 64 rows,
 //               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile and an S
 //               buffer are ready;
-//   warp 9      issues O^T += V^T . P^T (M = 128 dims x4, N = 64 heads, K = 64 rows) as soon as P is
-//               ready. Two issuers keep QK of the next tiles from queueing behind PV of the current
-//               one. The same tile is the K-major B of QK and, read MN-major, the A of PV, so it is
-//               dequantised once. Producers load and dequantise the next tile into registers
-//               while they wait for a free stage, so global-memory latency is off the MMA chain;
-//   warps 10-13 first convert Q's latent dims to fp16 in shared memory, then run the online
+//   warps 9-12  first convert Q's latent dims to fp16 in shared memory, then run the online
 //               softmax: two threads share each head's row of S (one shuffle for the max); P goes
 //               as fp16 into the stage's RoPE block, which QK no longer needs, so P is double
-//               buffered with the stages. O^T lives in TMEM and is rescaled only
-//               when a head's running max grows by more than 2^8 (lazy rescaling); the final pass
-//               divides by the row sum and writes bf16 straight from TMEM (neighbouring lanes swap
-//               values so that each stores two adjacent dims of one head).
+//               buffered with the stages. The last of the four warps to finish a tile (a counter
+//               in shared memory) issues O^T += V^T . P^T itself (M = 128 dims x4, N = 64 heads,
+//               K = 64 rows), so PV starts without a barrier hand-off to another warp, and QK of
+//               the next tiles, issued by warp 8, does not queue behind it. The same tile is the
+//               K-major B of QK and, read MN-major, the A of PV, so it is dequantised once. O^T
+//               lives in TMEM and is rescaled only when a head's running max grows by more than
+//               2^8 (lazy rescaling); the final pass divides by the row sum and writes bf16
+//               straight from TMEM (neighbouring lanes swap values so that each stores two
+//               adjacent dims of one head).
 // TMEM: columns 0-127 hold two S buffers (64-row layout), 128-383 hold O^T.
 //
 // Work split (launch_mla): one CTA per query when the queries fill their waves; otherwise, given a
@@ -44,9 +46,8 @@ namespace mla {
 constexpr int kRows = 64;
 constexpr int kProdWarps = 8;
 constexpr int kMmaWarp = kProdWarps;       // QK issuer; also allocates TMEM
-constexpr int kPvWarp = kProdWarps + 1;    // PV issuer
-constexpr int kSmThreads = 128;
-constexpr int kThreads = 32 * (kProdWarps + 2 + 4);
+constexpr int kSmThreads = 128;            // softmax / epilogue warps; the last one done with a tile issues its PV
+constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
 constexpr int kBlk = 8192;                 // one [64 rows][128 B] swizzled block
@@ -59,9 +60,9 @@ constexpr int kOffValid = kOffStage + 2 * kStageBytes;  // uint8 [2][64]
 constexpr int kOffAlpha = kOffValid + 128;          // float [64]
 constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
 constexpr int kEmpty = 5;                 // per stage: 4 latent block pairs (one PV M-tile each) + RoPE/P
-constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 12;
+constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 10;
 constexpr int kOffBar = kOffInvL + 256;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort
+constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort, P counter
 constexpr int kSmem = kOffMisc + 16 + 1024;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
@@ -111,6 +112,15 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t w0, uint32_t w1, uint32_t
   return r;
 }
 
+// One softmax warp's arrival on the tile counter (four per tile); true for the last of the four.
+// Each warp's P stores (already fenced for the async proxy) and TMEM accesses precede its release,
+// and the last arriver acquires them all before it issues the tile's PV.
+__device__ __forceinline__ bool arrive_last(uint32_t* ctr) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(ctr)) : "memory");
+  return (old & 3u) == 3u;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mla_kernel(const __grid_constant__ CUtensorMap map_q, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -125,16 +135,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = bars + 2 * kBlocks;      // [2][5] PV done with block pair m (m = 4: RoPE/P) -> producers
   uint64_t* s_full = empty + 2 * kEmpty;     // [2] QK done -> softmax
   uint64_t* s_free = s_full + 2;             // [2] softmax read S -> MMA
-  uint64_t* p_ready = s_full + 4;            // softmax wrote P (and corrected O) -> MMA
-  uint64_t* pv_done = s_full + 5;            // PV done -> softmax
-  uint64_t* q_full = s_full + 6;
-  uint64_t* mma_done = s_full + 7;           // QK issuer's MMAs drained
-  uint64_t* pv_drain = s_full + 8;           // PV issuer's MMAs drained
-  uint64_t* q_ready = s_full + 9;            // Q converted to fp16 (latent dims) -> QK issuer
-  uint64_t* q_free = s_full + 10;            // QK MMAs of a query finished reading Q -> QK issuer
-  uint64_t* o_free = s_full + 11;            // softmax read O^T of a query -> PV issuer
+  uint64_t* pv_done = s_full + 4;            // PV done -> softmax
+  uint64_t* q_full = s_full + 5;
+  uint64_t* mma_done = s_full + 6;           // QK issuer's MMAs drained
+  uint64_t* pv_drain = s_full + 7;           // PV MMAs of every softmax warp drained
+  uint64_t* q_ready = s_full + 8;            // Q converted to fp16 (latent dims) -> QK issuer
+  uint64_t* q_free = s_full + 9;             // QK MMAs of a query finished reading Q -> QK issuer
   uint32_t* misc = (uint32_t*)(smem + kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
+  uint32_t* p_count = misc + 2;              // softmax warps' tile completions (4 per tile)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k = p.k;
@@ -158,16 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
     }
-    mbar_init(p_ready, 4);
     mbar_init(pv_done, 1);
     mbar_init(q_full, 1);
     mbar_init(mma_done, 1);
-    mbar_init(pv_drain, 1);
+    mbar_init(pv_drain, kSmThreads / 32);
     mbar_init(q_ready, 4);
     mbar_init(q_free, 1);
-    mbar_init(o_free, 4);
     mbar_fence_init();
     misc[1] = 0;
+    misc[2] = 0;
   }
   if (warp == kMmaWarp) tmem_alloc(&misc[0], 512);
   __syncthreads();
@@ -391,50 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(mma_done, 0, p.err);
       if (seg > 0) mbar_wait(q_full, (uint32_t)(seg - 1) & 1u, p.err);  // the last Q copy has landed
     }
-  } else if (warp == kPvWarp) {
-    // ================================================================ PV issuer =================
-    if (lane == 0) {
-      constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
-      const uint32_t st_addr = smem_u32(sStage);
-      bool ok = true;
-      int seg = 0, j = 0;  // segment and global tile counters
-#pragma unroll 1
-      for (int64_t u = u0; u < u1 && ok; ++seg) {
-        const int64_t q = u / ntq;
-        const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
-        u = q * ntq + tb;
-        // O^T of the previous query must have been read out before it is overwritten
-        if (seg > 0 && !mbar_wait(o_free, (uint32_t)(seg - 1) & 1u, p.err)) {
-          ok = false;
-          break;
-        }
-#pragma unroll 1
-      for (int jt = ta; jt < tb; ++jt, ++j) {
-        if (*abort_flag || !mbar_wait(p_ready, (uint32_t)j & 1u, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = st_addr + (uint32_t)((j & 1) * kStageBytes);
-        const uint32_t p_addr = sa + 8 * kBlk;  // P of this tile in the stage's RoPE block
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = smem_desc(sa + (uint32_t)(2 * mt * kBlk + kk * 2048), kBlk, 1024, 2);
-            const uint64_t b = smem_desc(p_addr + kk * 32, 16, 1024, 2);
-            mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (jt > ta || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&empty[(j & 1) * kEmpty + mt]);  // dim blocks 2mt, 2mt+1 may be refilled
-        }
-        mma_commit(pv_done);
-        mma_commit(&empty[(j & 1) * kEmpty + 4]);     // P (the RoPE block) consumed
-      }
-      }
-      if (!ok) *abort_flag = 1;
-      mma_commit(pv_drain);
-      mbar_wait(pv_drain, 0, p.err);
-    }
   } else {
     // ================================================================ softmax / epilogue ========
     // Head h = 16 * quad + (lane % 16); lanes l and l + 16 share it, each owning 32 of the
@@ -443,6 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hl = lane & 15, half = lane >> 4;
     const int h = quad * 16 + hl;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
+    const uint32_t st_addr = smem_u32(sStage);
     bool ok = true;
     int seg = 0, i = 0;  // segment and global tile counters
 #pragma unroll 1
@@ -570,10 +536,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
+        // P and the corrected O^T are ready once all four warps are here; so is O^T of the previous
+        // query, read out by every warp before its first arrival for this one
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_ready);
+        if (lane == 0 && arrive_last(p_count)) {
+          // O^T += V^T . P^T: the stage read MN-major as A (M = 128 dims x4), P^T as B (N = 64 heads)
+          tc_fence_after();
+          const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
+          const uint32_t p_addr = sa + 8 * kBlk;  // P of this tile in the stage's RoPE block
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = smem_desc(sa + (uint32_t)(2 * mt * kBlk + kk * 2048), kBlk, 1024, 2);
+              const uint64_t b = smem_desc(p_addr + kk * 32, 16, 1024, 2);
+              mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (jt > ta || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&empty[s * kEmpty + mt]);  // dim blocks 2mt, 2mt+1 may be refilled
+          }
+          mma_commit(pv_done);
+          mma_commit(&empty[s * kEmpty + 4]);     // P (the RoPE block) consumed
+        }
       }
       // ---- the query's normalisation and output (final, or a partial for the merge) ----
       if (ok) {
@@ -626,10 +611,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // O^T has been read out: the next query's first PV may overwrite it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+    }
+    // the PV MMAs this warp issued have completed before TMEM is released
+    if (lane == 0) {
+      mma_commit(pv_drain);
+      mbar_wait(pv_drain, 0, p.err);
     }
   }
   __syncthreads();
