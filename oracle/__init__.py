@@ -8,6 +8,9 @@ which holds none of the method's arithmetic.
 Each function takes numpy arrays laid out exactly as the C ABI of the CUDA library (see
 ``include/hs.h``) and returns float64 results computed by the plain definitions in
 ``oracle.c``. ``threads=0`` uses every online core.
+
+Pages cited here besides those listed in ``oracle.c``:
+  [P4] "vLLMによるNVIDIA B300 GPU上でのGLM-5.2のサービング"
 """
 from __future__ import annotations
 
@@ -144,6 +147,28 @@ def sparse_mla(q_bits, kv_pool, idx, softmax_scale: float, block_table=None, tok
     if st:
         raise OracleError("sparse_mla: row out of range")
     return out, lse
+
+
+def shared_index_sets(idx, idx_row, token_kvlen=None) -> np.ndarray:
+    """int32 [T, k]: the index set each query token attends when the query tokens of a request
+    share one set.
+
+    [P4] section 「MTP受理率の安定化」: the indexer's top-k indices are reused rather than re-running
+    the indexer for every MTP token, and the shared index buffer of a batch keeps only each
+    request's final query token's indices. Query t takes row ``idx_row[t]`` of ``idx`` [rows, k];
+    with ``token_kvlen`` (logical indices), an entry j >= token_kvlen[t] is a token that query t
+    may not see (a later draft position) and becomes -1 padding. Raises OracleError for a row
+    outside idx.
+    """
+    idx = np.asarray(idx, dtype=np.int32)
+    idx_row = np.asarray(idx_row, dtype=np.int64)
+    if idx_row.size and (idx_row.min() < 0 or idx_row.max() >= idx.shape[0]):
+        raise OracleError("shared_index_sets: idx_row outside idx")
+    out = idx[idx_row].copy()
+    if token_kvlen is not None:
+        n = np.asarray(token_kvlen, dtype=np.int64)[:, None]
+        out[out >= n] = -1
+    return out
 
 
 def hisparse_resolve(step: int, idx, seq_len, resident_start, block_table, host_rows, kv_pool,

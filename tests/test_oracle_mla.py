@@ -112,3 +112,57 @@ def test_out_of_range_row_rejected():
     rows = _rows(np.zeros((2, 512)), np.zeros((2, 64)), np.ones((2, 4)))
     with pytest.raises(oracle.OracleError):
         oracle.sparse_mla(np.zeros((1, 1, 576), np.uint16), rows, np.array([[0, 2]], np.int32), 1.0)
+
+
+def test_shared_index_sets_hand_case():
+    """One request's set [0, 5, 9, -1] shared by three tokens that see 3, 6 and 10 tokens: each
+    keeps the entries it can see (worked by hand)."""
+    idx = np.array([[0, 5, 9, -1], [7, 7, 1, 2]], np.int32)
+    got = oracle.shared_index_sets(idx, np.array([0, 0, 0, 1]), np.array([3, 6, 10, 2]))
+    want = np.array([[0, -1, -1, -1], [0, 5, -1, -1], [0, 5, 9, -1], [-1, -1, 1, -1]], np.int32)
+    assert np.array_equal(got, want)
+    # without a limit the rows are copied as they are
+    assert np.array_equal(oracle.shared_index_sets(idx, np.array([1, 0])), idx[::-1])
+    with pytest.raises(oracle.OracleError):
+        oracle.shared_index_sets(idx, np.array([0, 2]))
+
+
+def test_shared_sets_give_causal_attention_for_every_mtp_token():
+    """Two requests decode 1 + 3 MTP tokens each; all four share the set of the final token.
+    When that set holds every token of the request (in any order, padded), token i at position
+    p must attend exactly the tokens at positions <= p: dense causal attention, here torch's
+    scaled_dot_product_attention with a position mask."""
+    st = inputs.Stream(41)
+    ctx = np.array([150, 97], np.int32)
+    bt, nblk = inputs.paged_block_tables(ctx, st.sub("bt"))
+    tok_rows = inputs.pack_kv_rows(st.sub("l").normal((int(ctx.sum()), 512)), st.sub("r").normal((int(ctx.sum()), 64)))
+    pool = inputs.scatter_paged(tok_rows, ctx, bt, nblk)
+    H, k = 3, 160
+    token_req = np.repeat(np.arange(2, dtype=np.int32), 4)
+    pos = np.concatenate([c - 4 + np.arange(4) for c in ctx]).astype(np.int32)
+    g = st.sub("perm").gen()
+    final = np.full((2, k), -1, np.int32)
+    for r, c in enumerate(ctx):
+        final[r, :c] = g.permutation(int(c))
+        final[r] = final[r][g.permutation(k)]  # padding anywhere
+    sets = oracle.shared_index_sets(final, token_req, pos + 1)
+    q = inputs.bf16_bits(st.sub("q").normal((8, H, 576), sigma=0.5))
+    scale = 1 / math.sqrt(576)
+    out, lse = oracle.sparse_mla(q, pool, sets, scale, block_table=bt, token_req=token_req)
+    lat, rope = _decode_rows(tok_rows)
+    Q = _q64(q)
+    off = np.concatenate([[0], np.cumsum(ctx)[:-1]])
+    for t in range(8):
+        r = token_req[t]
+        K = torch.cat([lat, rope], dim=1)[off[r]:off[r] + ctx[r]]
+        V = lat[off[r]:off[r] + ctx[r]]
+        mask = (torch.arange(int(ctx[r])) <= int(pos[t]))[None, None, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Q[t][None, :, None, :], K[None, None].expand(1, H, -1, 576), V[None, None].expand(1, H, -1, 512),
+            attn_mask=mask, scale=scale)
+        assert np.allclose(out[t], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12), t
+        logits = (Q[t] @ K.T) * scale
+        logits[:, int(pos[t]) + 1:] = -math.inf
+        assert np.allclose(lse[t], torch.logsumexp(logits, dim=1).numpy(), rtol=1e-12, atol=1e-12), t
+    # the final token of each request sees its whole set
+    assert np.array_equal(sets[3], final[0]) and np.array_equal(sets[7], final[1])
