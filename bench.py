@@ -172,27 +172,45 @@ def build_workload(config: int, seed: int, requests: int = 64):
     raise SystemExit("--config %d: use 1, 2 or 3 for the indexer/top-k/MLA step (4, 5: analysis modes)" % config)
 
 
-def work_of(w):
+def final_tokens(w):
+    """Index of each request's final query token (the one that sees the most tokens)."""
+    return np.array([np.flatnonzero(w.token_req == r)[np.argmax(w.token_kvlen[w.token_req == r])]
+                     for r in np.unique(w.token_req)])
+
+
+def work_of(w, shared=False):
+    """Algorithmic work per step. With shared index sets the indexer and top-k run for each
+    request's final token only; attention rows are counted as min(n_t, k) per token either way
+    (with a shared set a token may see up to three fewer)."""
     from dsa_sparse_mla_gb300 import costmodel as cm
-    kvsum = int(w.token_kvlen.astype(np.int64).sum())
+    sel = final_tokens(w) if shared else np.arange(w.T)
+    kvsum = int(w.token_kvlen[sel].astype(np.int64).sum())
     ctxsum = int(w.ctx.astype(np.int64).sum())
     rows = int(np.minimum(w.token_kvlen, w.topk).astype(np.int64).sum())
-    return {"indexer": cm.indexer_work(w.Hi, w.Di, kvsum, ctxsum, w.T), "topk": cm.topk_work(kvsum, w.T, w.topk),
-            "mla": cm.mla_work(w.H, rows, w.T)}
+    return {"indexer": cm.indexer_work(w.Hi, w.Di, kvsum, ctxsum, len(sel)),
+            "topk": cm.topk_work(kvsum, len(sel), w.topk), "mla": cm.mla_work(w.H, rows, w.T)}
 
 
 # ------------------------------------------------------------------------ CPU oracle ---------
 
-def oracle_sample(w, tokens, threads=0):
+def oracle_sample(w, tokens, threads=0, shared=False):
     """Runs the CPU oracle (indexer -> top-k -> sparse MLA) on the given query tokens; returns
-    the wall time in seconds."""
+    the wall time in seconds. With shared index sets the indexer and top-k run for the final
+    token of each request among them, and every token attends its request's set."""
     import oracle
     rows = np.asarray(tokens)
     sl = lambda a: np.ascontiguousarray(a[rows])
+    sel = rows
+    if shared:
+        fin = set(final_tokens(w).tolist())
+        sel = np.array([t for t in rows if t in fin])
+    sf = lambda a: np.ascontiguousarray(a[sel])
     t0 = time.perf_counter()
-    s = oracle.indexer_scores(sl(w.q_idx), sl(w.q_scale), sl(w.weights), w.k_cache, w.k_scale, w.block_table,
-                              sl(w.token_req), sl(w.token_kvlen), ld=w.ld, threads=threads)
-    idx = oracle.topk(s, sl(w.token_kvlen), w.topk, threads=threads)
+    s = oracle.indexer_scores(sf(w.q_idx), sf(w.q_scale), sf(w.weights), w.k_cache, w.k_scale, w.block_table,
+                              sf(w.token_req), sf(w.token_kvlen), ld=w.ld, threads=threads)
+    idx = oracle.topk(s, sf(w.token_kvlen), w.topk, threads=threads)
+    if shared:
+        idx = oracle.shared_index_sets(idx, np.searchsorted(w.token_req[sel], w.token_req[rows]), sl(w.token_kvlen))
     oracle.sparse_mla(sl(w.q_mla), w.kv_pool, idx, w.softmax_scale, w.block_table, sl(w.token_req), threads=threads)
     return time.perf_counter() - t0
 
@@ -221,16 +239,18 @@ def run_ours(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
     import dsa_sparse_mla_gb300 as hs
-    from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
+    from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath, SharedSetHotPath
 
     hs.load()
     peaks, peaks_kind = load_peaks()
     w = build_workload(args.config, rank_seed(args.config, rank), args.requests)
     dw = DeviceWorkload.from_host(w, dev)
-    hp = HotPath(dw)
+    Path = SharedSetHotPath if args.shared_sets else HotPath
+    hp = Path(dw)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    work = work_of(w)
+    work = work_of(w, args.shared_sets)
+    wl_name = w.name + ("-shared-sets" if args.shared_sets else "")
 
     for _ in range(args.warmup):
         hp.step()
@@ -271,11 +291,10 @@ def run_ours(args):
     # two buffer sets, so step i + 1's inputs and step i - 1's outputs move while step i computes,
     # as a serving loop would run them. No L2 flush: the K cache and KV pool are larger than L2.
     import dataclasses
-    from dsa_sparse_mla_gb300.pipeline import HotPath
     names_in = ("q_idx", "q_scale", "weights", "q_mla", "token_req", "token_kvlen")
-    h_in = [getattr(dw, nm).cpu().pin_memory() for nm in names_in]
+    h_in = [t.cpu().pin_memory() for t in hp.step_inputs()]
     dws = [dw, dataclasses.replace(dw, **{nm: torch.empty_like(getattr(dw, nm)) for nm in names_in})]
-    hps = [hp, HotPath(dws[1])]
+    hps = [hp, Path(dws[1])]
     h_out = [[torch.empty_like(hp.out, device="cpu").pin_memory(), torch.empty_like(hp.lse, device="cpu").pin_memory()]
              for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
@@ -291,8 +310,8 @@ def run_ours(args):
         with torch.cuda.stream(cstream):
             if i >= 2:
                 cstream.wait_event(step_done[st])  # step i - 2 read this set's inputs
-            for nm, h in zip(names_in, h_in):
-                getattr(dws[st], nm).copy_(h, non_blocking=True)
+            for dst, h in zip(hps[st].step_inputs(), h_in):
+                dst.copy_(h, non_blocking=True)
             in_ready[st].record(cstream)
 
     def copy_out(i):
@@ -364,7 +383,7 @@ def run_ours(args):
     roof["kernel"] = dom
     roof["peak_source"] = ("%s (MEASURED_PEAKS.json)" % peaks_kind) + (
         "; fp8 = sustained bf16 x nominal 2" if (dom == "indexer" and not bytes_bound) else "")
-    roof["traffic"] = recorded_traffic(dom, w.name)
+    roof["traffic"] = recorded_traffic(dom, wl_name)
     layer_roof_ms = sum(kern[n]["roofline_ms"] for n in kern)
 
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
@@ -376,7 +395,7 @@ def run_ours(args):
         sample = list(range(w.T))
         wall_cpu, passes = 0.0, 0
         while passes < 4 and (passes == 0 or wall_cpu < 10.0):
-            wall_cpu += oracle_sample(w, sample, threads=0)
+            wall_cpu += oracle_sample(w, sample, threads=0, shared=args.shared_sets)
             passes += 1
         cpu = {"value": round(passes * len(sample) / wall_cpu, 3), "unit": "tokens/s",
                "cores": min(threads, len(sample)), "kind": "oracle",
@@ -386,10 +405,12 @@ def run_ours(args):
     line = {"metric": METRIC, "value": round(tokens / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16", "data": "synthetic",
-            "config": {"workload": w.name, "requests": w.B, "query_tokens": w.T,
+            "config": {"workload": wl_name, "requests": w.B, "query_tokens": w.T,
                        "ctx": "U{16384..65536}" if args.config == 2 else int(w.ctx.max()),
                        "index_heads": w.Hi, "index_dim": w.Di, "topk": w.topk, "mla_heads": w.H, "page": 64,
-                       "l2": "256 MB write between timed steps (inputs also > L2)", "parallelism": "dp%d" % world},
+                       "l2": "256 MB write between timed steps (inputs also > L2)", "parallelism": "dp%d" % world,
+                       "index_sets": ("shared: each request's final query token's top-k, reused by its other query "
+                                      "tokens up to their own visible length") if args.shared_sets else "per query token"},
             "roofline": roof,
             "layer_roofline_frac": round(layer_roof_ms / tot, 4),
             "kernels": kern,
@@ -655,6 +676,9 @@ def main(argv=None):
     ap.add_argument("--hisparse-steps", type=int, default=50, help="--config 5: decode steps")
     ap.add_argument("--kv-append", type=int, default=0, help="time hs_kv_append on this many new tokens instead")
     ap.add_argument("--kv-offload", type=int, default=0, help="time hs_kv_offload on about this many pages instead")
+    ap.add_argument("--shared-sets", action="store_true",
+                    help="the query tokens of a request share its final token's index set (indexer and top-k "
+                         "run for final tokens only)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -46,7 +46,8 @@ class _IndexerArgs(ctypes.Structure):
 class _MlaArgs(ctypes.Structure):
     _fields_ = [("T", _i32), ("H", _i32), ("k", _i32), ("q", _P), ("kv_pool", _P), ("R", _i64), ("idx", _P),
                 ("block_table", _P), ("bt_stride", _i32), ("token_req", _P), ("softmax_scale", _f32),
-                ("out", _P), ("lse", _P), ("err_flag", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_uint64)]
+                ("out", _P), ("lse", _P), ("err_flag", _P), ("workspace", _P), ("workspace_bytes", ctypes.c_uint64),
+                ("idx_row", _P), ("idx_rows", _i32), ("token_kvlen", _P)]
 
 
 class _ResolveArgs(ctypes.Structure):
@@ -161,38 +162,44 @@ def hs_sparse_mla_workspace_size(H: int) -> int:
     return int(n.value)
 
 
-def hs_sparse_mla_fwd(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=None, block_table=None,
-                      token_req=None, workspace=None, stream=None):
-    """Sparse MLA forward: ``out`` bf16 [T, H, 512] (and ``lse`` float32 [T, H] if given). With a
-    ``workspace`` (uint8 CUDA tensor of at least hs_sparse_mla_workspace_size(H) bytes) every SM
-    gets an equal share of the work and split queries are merged by log-sum-exp."""
+def _mla_args(q, kv_pool, idx, softmax_scale, out, err_flag, lse, block_table, token_req, workspace, idx_row,
+              token_kvlen):
     _dev(q, "q", torch.bfloat16), _dev(kv_pool, "kv_pool", torch.uint8), _dev(idx, "idx", torch.int32)
     _dev(workspace, "workspace", torch.uint8)
     _dev(out, "out", torch.bfloat16), _dev(err_flag, "err_flag", torch.int32), _dev(lse, "lse", torch.float32)
     _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
+    _dev(idx_row, "idx_row", torch.int32), _dev(token_kvlen, "token_kvlen", torch.int32)
     T, H, D = q.shape
-    if D != 576 or kv_pool.shape[-1] != 656 or out.shape != (T, H, 512) or idx.shape[0] != T:
-        raise HSError(1, "shape mismatch: q [T,H,576], kv_pool [R,656], idx [T,k], out [T,H,512]")
-    a = _MlaArgs(T, H, idx.shape[1], _ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(idx), _ptr(block_table),
-                 0 if block_table is None else block_table.shape[1], _ptr(token_req), float(softmax_scale),
-                 _ptr(out), _ptr(lse), _ptr(err_flag), _ptr(workspace),
-                 0 if workspace is None else workspace.numel())
+    if D != 576 or kv_pool.shape[-1] != 656 or out.shape != (T, H, 512) or (idx_row is None and idx.shape[0] != T):
+        raise HSError(1, "shape mismatch: q [T,H,576], kv_pool [R,656], idx [T,k] (or [rows,k] with idx_row), "
+                         "out [T,H,512]")
+    for t, n in ((idx_row, "idx_row"), (token_kvlen, "token_kvlen")):
+        if t is not None and t.shape != (T,):
+            raise HSError(1, "%s must be int32 [T]" % n)
+    return _MlaArgs(T, H, idx.shape[1], _ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(idx), _ptr(block_table),
+                    0 if block_table is None else block_table.shape[1], _ptr(token_req), float(softmax_scale),
+                    _ptr(out), _ptr(lse), _ptr(err_flag), _ptr(workspace),
+                    0 if workspace is None else workspace.numel(), _ptr(idx_row), idx.shape[0], _ptr(token_kvlen))
+
+
+def hs_sparse_mla_fwd(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=None, block_table=None,
+                      token_req=None, workspace=None, stream=None, idx_row=None, token_kvlen=None):
+    """Sparse MLA forward: ``out`` bf16 [T, H, 512] (and ``lse`` float32 [T, H] if given). With a
+    ``workspace`` (uint8 CUDA tensor of at least hs_sparse_mla_workspace_size(H) bytes) every SM
+    gets an equal share of the work and split queries are merged by log-sum-exp. Shared index sets:
+    ``idx_row`` (int32 [T]) names the row of ``idx`` each query reads, and ``token_kvlen`` (int32
+    [T], with a block table) skips the entries a query may not see."""
+    a = _mla_args(q, kv_pool, idx, softmax_scale, out, err_flag, lse, block_table, token_req, workspace, idx_row,
+                  token_kvlen)
     _check(load().hs_sparse_mla_fwd(ctypes.byref(a), _stream(stream)))
 
 
 def hs_sparse_mla_fwd_static(q, kv_pool, idx, softmax_scale: float, out, err_flag, lse=None, block_table=None,
-                             token_req=None, stream=None):
+                             token_req=None, stream=None, idx_row=None, token_kvlen=None):
     """hs_sparse_mla_fwd for callers that cannot allocate device memory: the split-work scratch is
     the library's own fixed device array (see include/hs.h), so no workspace is passed."""
-    _dev(q, "q", torch.bfloat16), _dev(kv_pool, "kv_pool", torch.uint8), _dev(idx, "idx", torch.int32)
-    _dev(out, "out", torch.bfloat16), _dev(err_flag, "err_flag", torch.int32), _dev(lse, "lse", torch.float32)
-    _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
-    T, H, D = q.shape
-    if D != 576 or kv_pool.shape[-1] != 656 or out.shape != (T, H, 512) or idx.shape[0] != T:
-        raise HSError(1, "shape mismatch: q [T,H,576], kv_pool [R,656], idx [T,k], out [T,H,512]")
-    a = _MlaArgs(T, H, idx.shape[1], _ptr(q), _ptr(kv_pool), kv_pool.shape[0], _ptr(idx), _ptr(block_table),
-                 0 if block_table is None else block_table.shape[1], _ptr(token_req), float(softmax_scale),
-                 _ptr(out), _ptr(lse), _ptr(err_flag), None, 0)
+    a = _mla_args(q, kv_pool, idx, softmax_scale, out, err_flag, lse, block_table, token_req, None, idx_row,
+                  token_kvlen)
     _check(load().hs_sparse_mla_fwd_static(ctypes.byref(a), _stream(stream)))
 
 

@@ -155,6 +155,8 @@ hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream) {
   REQUIRE(aligned16(a->q) && aligned16(a->kv_pool), "q and kv_pool must be 16-byte aligned");
   REQUIRE(a->R >= 1, "R must be >= 1");
   REQUIRE(!a->block_table || (a->token_req && a->bt_stride >= 1), "block_table needs token_req and bt_stride >= 1");
+  REQUIRE(!a->idx_row || a->idx_rows >= 1, "idx_row needs idx_rows >= 1");
+  REQUIRE(!a->token_kvlen || a->block_table, "token_kvlen needs block_table (it limits logical token indices)");
   REQUIRE((int64_t)a->T * a->H <= INT32_MAX && (int64_t)a->T * a->k <= ((int64_t)1 << 40), "T * H or T * k too large");
   REQUIRE(a->softmax_scale == a->softmax_scale, "softmax_scale is NaN");
   int sms = 0;

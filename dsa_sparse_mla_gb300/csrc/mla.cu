@@ -76,6 +76,9 @@ struct Params {
   const uint8_t* kv;
   int64_t R;
   const int32_t* idx;
+  const int32_t* idx_row;  // shared index sets: query t reads idx row idx_row[t] (NULL: row t)
+  int32_t idx_rows;
+  const int32_t* kvlen;    // entries j >= kvlen[t] are skipped (NULL: none)
   const int32_t* bt;
   int32_t bt_stride;
   const int32_t* token_req;
@@ -212,9 +215,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++la_q;
       }
       ++la_n;
-      if (lane >= 8 || !live) return -1;
+      if (lane >= 8 || !live || e >= k) return -1;
+      int64_t row = q;
+      if (p.idx_row) {
+        row = ldg_nc_s32(p.idx_row + q);
+        if (row < 0 || row >= p.idx_rows) {
+          flag_error(p.err, HS_FLAG_BAD_INDEX);
+          return -1;
+        }
+      }
       if (p.bt) req = ldg_nc_s32(p.token_req + q);
-      return e < k ? ldg_nc_s32(p.idx + q * k + e) : -1;
+      const int32_t j = ldg_nc_s32(p.idx + row * k + e);
+      return p.kvlen && j >= ldg_nc_s32(p.kvlen + q) ? -1 : j;
     };
     auto ld_blk = [&](int32_t j, int32_t req) -> int32_t {  // lanes 0-7: block-table entry of entry j (j if none)
       if (lane >= 8 || j < 0 || !p.bt) return j;
@@ -744,6 +756,9 @@ cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const
   p.kv = a->kv_pool;
   p.R = a->R;
   p.idx = a->idx;
+  p.idx_row = a->idx_row;
+  p.idx_rows = a->idx_rows;
+  p.kvlen = a->token_kvlen;
   p.bt = a->block_table;
   p.bt_stride = a->bt_stride;
   p.token_req = a->token_req;

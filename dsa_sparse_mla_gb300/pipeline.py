@@ -2,7 +2,9 @@
 
 ``DeviceWorkload`` moves a seeded ``inputs.Workload`` into GPU memory; ``HotPath`` owns the
 intermediate and output buffers and runs one step: hs_indexer_scores -> hs_topk ->
-hs_sparse_mla_fwd (logical indices through the paged block table). ``DeviceHiSparse`` does the
+hs_sparse_mla_fwd (logical indices through the paged block table); ``SharedSetHotPath`` runs the
+indexer and top-k for each request's final query token only and lets the request's other query
+tokens reuse that set in hs_sparse_mla_fwd (shared index sets). ``DeviceHiSparse`` does the
 same for the mixed-residency decode (hs_hisparse_resolve -> hs_sparse_mla_fwd on physical rows),
 with the older rows in pinned host memory.
 
@@ -64,6 +66,12 @@ class HotPath:
         # sparse-MLA scratch: every SM gets an equal share of the (query, tile) work
         self.workspace = torch.empty(hs_sparse_mla_workspace_size(w.H), dtype=torch.uint8, device=dev)
 
+    def step_inputs(self) -> list:
+        """The device tensors a step reads that change from step to step (a serving loop copies
+        them in); everything else (caches, block tables, pools) stays resident."""
+        d = self.dw
+        return [d.q_idx, d.q_scale, d.weights, d.q_mla, d.token_req, d.token_kvlen]
+
     def indexer(self, stream=None):
         d = self.dw
         hs_indexer_scores(d.q_idx, d.q_scale, d.weights, d.k_cache, d.k_scale, d.block_table, d.token_req,
@@ -81,6 +89,50 @@ class HotPath:
         self.indexer(stream)
         self.topk(stream)
         self.mla(stream)
+
+
+class SharedSetHotPath(HotPath):
+    """One step with shared index sets: hs_indexer_scores and hs_topk run for the final query token
+    of each request only, and hs_sparse_mla_fwd gives every query token its request's set
+    (idx_row), limited to the tokens it can see (token_kvlen), so MTP tokens do not re-run the
+    indexer."""
+
+    def __init__(self, dw: DeviceWorkload):
+        super().__init__(dw)
+        w = dw.w
+        dev = dw.q_idx.device
+        req = np.asarray(w.token_req)
+        last = np.array([np.flatnonzero(req == r)[np.argmax(w.token_kvlen[req == r])] for r in np.unique(req)])
+        row_of_req = np.full(int(req.max()) + 1, -1, np.int32)
+        row_of_req[req[last]] = np.arange(len(last), dtype=np.int32)
+        li = torch.from_numpy(last).to(dev)
+        self.f_q_idx, self.f_q_scale, self.f_weights = (dw.q_idx[li].contiguous(), dw.q_scale[li].contiguous(),
+                                                        dw.weights[li].contiguous())
+        self.f_req, self.f_kvlen = dw.token_req[li].contiguous(), dw.token_kvlen[li].contiguous()
+        self.idx_row = _t(row_of_req[req], dev)
+        self.scores = torch.empty((len(last), w.ld), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((len(last), w.topk), dtype=torch.int32, device=dev)
+
+    def step_inputs(self) -> list:
+        """Only the final tokens' indexer inputs change per step here, with every token's MLA query
+        and the token-to-request, visible-length and index-row maps."""
+        d = self.dw
+        return [self.f_q_idx, self.f_q_scale, self.f_weights, self.f_req, self.f_kvlen, self.idx_row, d.q_mla,
+                d.token_req, d.token_kvlen]
+
+    def indexer(self, stream=None):
+        d = self.dw
+        hs_indexer_scores(self.f_q_idx, self.f_q_scale, self.f_weights, d.k_cache, d.k_scale, d.block_table,
+                          self.f_req, self.f_kvlen, self.scores, self.err, num_requests=d.w.B, stream=stream)
+
+    def topk(self, stream=None):
+        hs_topk(self.scores, self.f_kvlen, self.dw.w.topk, self.idx, self.err, stream=stream)
+
+    def mla(self, stream=None):
+        d = self.dw
+        hs_sparse_mla_fwd(d.q_mla, d.kv_pool, self.idx, d.w.softmax_scale, self.out, self.err, lse=self.lse,
+                          block_table=d.block_table, token_req=d.token_req, workspace=self.workspace, stream=stream,
+                          idx_row=self.idx_row, token_kvlen=d.token_kvlen)
 
 
 def pinned_uint8(nbytes: int) -> np.ndarray:

@@ -86,7 +86,7 @@ typedef enum {
 #define HS_D_LATENT 512          /* latent (value) width */
 #define HS_D_ROPE 64             /* RoPE width */
 #define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
-#define HS_ABI_VERSION 5
+#define HS_ABI_VERSION 6
 
 int hs_abi_version(void);
 const char* hs_status_str(hs_status s);
@@ -186,12 +186,23 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  * (< R); otherwise logical token indices of request token_req[t] mapped through the paged layout.
  * A query with no valid entry gets out = 0 and lse = -inf. Each occurrence of a duplicated entry counts.
  *
+ * Shared index sets ([P4] 「MTP受理率の安定化」: the indexer's top-k indices are reused instead of
+ * re-running the indexer for every MTP token, and the shared index buffer of a batch keeps only
+ * each request's final query token's indices): with idx_row != NULL, query t reads index row
+ * idx_row[t] of idx [idx_rows, k] instead of row t, so the query tokens of a request can share the
+ * set selected for its final token. token_kvlen (with a block table only) is each query's count of
+ * visible tokens: entries j >= token_kvlen[t] are skipped, which keeps a shared set causal for the
+ * earlier tokens (they do not see the later draft positions the final token selected). An
+ * idx_row[t] outside [0, idx_rows) sets HS_FLAG_BAD_INDEX and the query gets no rows.
+ *
  *   T, H          query tokens; heads, 1 <= H <= 64
  *   k             entries per idx row
  *   q             bf16 [T, H, 576] (16-byte aligned)
  *   kv_pool       uint8 [R, 656] (16-byte aligned)
- *   idx           int32 [T, k]
+ *   idx           int32 [T, k], or [idx_rows, k] with idx_row
  *   block_table   int32 [B, bt_stride] or NULL; token_req int32 [T] (required with block_table)
+ *   idx_row       int32 [T] or NULL; idx_rows >= 1 rows of idx when given
+ *   token_kvlen   int32 [T] or NULL (needs block_table)
  *   out           bf16 [T, H, 512]
  *   lse           fp32 [T, H] or NULL
  *   workspace     NULL: one CTA per query token. Otherwise at least hs_sparse_mla_workspace_size()
@@ -219,6 +230,9 @@ typedef struct {
   int32_t* err_flag;
   void* workspace;           /* NULL, or caller-owned device scratch (see below) */
   uint64_t workspace_bytes;  /* its size in bytes */
+  const int32_t* idx_row;    /* NULL, or the idx row of each query (shared index sets) */
+  int32_t idx_rows;          /* rows of idx when idx_row is given */
+  const int32_t* token_kvlen;  /* NULL, or each query's visible tokens (entries >= it skipped) */
 } hs_mla_args;
 
 hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream);

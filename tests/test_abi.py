@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert hs.hs_abi_version() == 5
+    assert hs.hs_abi_version() == 6
     hs.load()
     for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                                  "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
@@ -53,6 +53,11 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     m = hs._MlaArgs()
     m.T, m.H, m.k = 1, 0, 1
     assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1
+    m.H, m.err_flag, m.q, m.kv_pool, m.idx, m.out, m.R = 1, 16, 16, 16, 16, 16, 1
+    m.idx_row, m.idx_rows = 16, 0                                     # shared rows, but none
+    assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1 and b"idx_rows" in L.hs_last_error()
+    m.idx_row, m.token_kvlen = None, 16                               # a causal limit without a block table
+    assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1 and b"token_kvlen needs" in L.hs_last_error()
     n = ctypes.c_uint64(0)
     assert L.hs_sparse_mla_workspace_size(0, ctypes.byref(n)) == 1 and b"H must be" in L.hs_last_error()
     r = hs._ResolveArgs()

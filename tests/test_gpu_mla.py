@@ -27,7 +27,7 @@ def _workspace(H):
     return torch.empty(hs_sparse_mla_workspace_size(H), dtype=torch.uint8, device="cuda")
 
 
-def _run(q_bits, kv, idx, scale, bt=None, req=None, split=False):
+def _run(q_bits, kv, idx, scale, bt=None, req=None, split=False, idx_row=None, kvlen=None):
     T, H, _ = q_bits.shape
     q = torch.from_numpy(q_bits.view(np.int16)).cuda().view(torch.bfloat16)
     kvt = torch.from_numpy(kv).cuda()
@@ -40,7 +40,10 @@ def _run(q_bits, kv, idx, scale, bt=None, req=None, split=False):
     ws = _workspace(H) if split else None
     if ws is not None:
         ws.fill_(0xFF)   # the workspace needs no initialisation: stale contents must not matter
-    hs_sparse_mla_fwd(q, kvt, it, scale, out, err, lse=lse, block_table=btt, token_req=rt, workspace=ws)
+    ir = None if idx_row is None else torch.from_numpy(np.ascontiguousarray(idx_row, np.int32)).cuda()
+    kl = None if kvlen is None else torch.from_numpy(np.ascontiguousarray(kvlen, np.int32)).cuda()
+    hs_sparse_mla_fwd(q, kvt, it, scale, out, err, lse=lse, block_table=btt, token_req=rt, workspace=ws,
+                      idx_row=ir, token_kvlen=kl)
     flag = hs_check_flag(err)
     return out, lse, flag
 
@@ -159,3 +162,52 @@ def test_out_of_fp16_range_scale_is_flagged():
     assert flag & 0x40
     _, _, flag = _run(q, kv, np.array([[0, 1, 2, 3]], np.int32), 0.05)
     assert flag == 0
+
+
+def _final_token_sets(w, rng):
+    """Per request, a top-k-sized set for its final query token that always holds the three
+    latest positions (the ones the earlier MTP tokens may not see), in random order."""
+    B = w.block_table.shape[0]
+    final = np.full((B, w.topk), -1, np.int32)
+    for r in range(B):
+        n = int(w.token_kvlen[w.token_req == r].max())
+        m = min(n - 3, w.topk - 3)
+        sel = np.concatenate([np.arange(n - 3, n), rng.choice(n - 3, size=m, replace=False)])
+        final[r, :len(sel)] = rng.permutation(sel)
+    return final
+
+
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("topk", [256, 2048])
+def test_shared_index_sets_across_mtp_tokens(topk, split):
+    """The four MTP tokens of a request attend its final token's set (idx_row), each limited to
+    the tokens it can see (token_kvlen): parity with the oracle on the expanded sets, and the same
+    bits as a call on those expanded sets."""
+    w = inputs.config2(seed=37, B=5, lo=300, hi=3000, Hi=8, Di=64, H=64, topk=topk)
+    final = _final_token_sets(w, np.random.default_rng(topk))
+    sets = oracle.shared_index_sets(final, w.token_req, w.token_kvlen)
+    assert (sets >= 0).sum() < 4 * (final >= 0).sum()   # the earlier tokens lost entries
+    out, lse, flag = _run(w.q_mla, w.kv_pool, final, w.softmax_scale, w.block_table, w.token_req, split=split,
+                          idx_row=w.token_req, kvlen=w.token_kvlen)
+    assert flag == 0
+    ref, lref = oracle.sparse_mla(w.q_mla, w.kv_pool, sets, w.softmax_scale, w.block_table, w.token_req)
+    check_mla(out, lse, ref, lref)
+    out2, lse2, flag2 = _run(w.q_mla, w.kv_pool, sets, w.softmax_scale, w.block_table, w.token_req, split=split)
+    assert flag2 == 0
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_shared_index_row_out_of_range_flagged():
+    """A query naming an idx row that does not exist gets no rows (out 0, lse -inf) and sets
+    HS_FLAG_BAD_INDEX; the other queries are unaffected."""
+    w = inputs.config2(seed=38, B=2, lo=300, hi=900, Hi=8, Di=64, H=16, topk=128)
+    final = _final_token_sets(w, np.random.default_rng(5))
+    rows = w.token_req.copy()
+    rows[2] = 2                                          # only rows 0 and 1 exist
+    out, lse, flag = _run(w.q_mla, w.kv_pool, final, w.softmax_scale, w.block_table, w.token_req,
+                          idx_row=rows, kvlen=w.token_kvlen)
+    assert flag & 0x01
+    sets = oracle.shared_index_sets(final, w.token_req, w.token_kvlen)
+    sets[2] = -1
+    ref, lref = oracle.sparse_mla(w.q_mla, w.kv_pool, sets, w.softmax_scale, w.block_table, w.token_req)
+    check_mla(out, lse, ref, lref)

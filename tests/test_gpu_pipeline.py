@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from dsa_sparse_mla_gb300 import hs_check_flag, inputs
-from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
+from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath, SharedSetHotPath
 
 from parity import check_mla, check_topk_sets
 
@@ -61,3 +61,26 @@ def test_repeat_is_deterministic():
     a = (hp.idx.clone(), hp.out.clone(), hp.lse.clone())
     hp.step()
     assert hp.idx.equal(a[0]) and hp.out.equal(a[1]) and hp.lse.equal(a[2])
+
+
+def test_mtp_decode_shared_sets_full_size_sampled():
+    """Shared index sets on the full MTP-decode batch: the indexer and top-k of each request's
+    final token against the oracle's, and every token of the sampled requests attending that set
+    (limited to what it can see) against the oracle on the expanded sets."""
+    w = inputs.config2()
+    hp = SharedSetHotPath(DeviceWorkload.from_host(w))
+    hp.step()
+    assert hs_check_flag(hp.err) == 0
+    reqs = np.array([0, 17, 63])
+    final = np.array([np.flatnonzero(w.token_req == r)[-1] for r in reqs])   # the last token of each request
+    sl = lambda a: np.ascontiguousarray(a[final])
+    idx_gpu = hp.idx.cpu().numpy()[reqs]
+    ref_scores = oracle.indexer_scores(sl(w.q_idx), sl(w.q_scale), sl(w.weights), w.k_cache, w.k_scale, w.block_table,
+                                       sl(w.token_req), sl(w.token_kvlen), ld=w.ld)
+    ref_idx = oracle.topk(ref_scores, sl(w.token_kvlen), w.topk)
+    check_topk_sets(idx_gpu, ref_scores, sl(w.token_kvlen), w.topk, ref_idx)
+    rows = np.flatnonzero(np.isin(w.token_req, reqs))
+    sets = oracle.shared_index_sets(idx_gpu, np.searchsorted(reqs, w.token_req[rows]), w.token_kvlen[rows])
+    out_ref, lse_ref = oracle.sparse_mla(np.ascontiguousarray(w.q_mla[rows]), w.kv_pool, sets, w.softmax_scale,
+                                         w.block_table, np.ascontiguousarray(w.token_req[rows]))
+    check_mla(hp.out[rows], hp.lse[rows], out_ref, lse_ref)
