@@ -66,7 +66,7 @@ typedef struct CUstream_st* hs_stream_t;
 typedef enum {
   HS_OK = 0,
   HS_ERR_INVALID = 1,      /* an argument failed the host-side checks; nothing was launched */
-  HS_ERR_UNSUPPORTED = 2,  /* valid request that this build cannot serve (device, size limit) */
+  HS_ERR_UNSUPPORTED = 2,  /* valid request that the library cannot serve (device, size limit) */
   HS_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed; see hs_last_error() */
   HS_ERR_DEVICE_FLAG = 4,  /* returned by hs_check_flag when the device error flag is non-zero */
   HS_ERR_TIMEOUT = 5       /* returned by hs_check_flag when HS_FLAG_TIMEOUT is set */
