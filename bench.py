@@ -389,7 +389,7 @@ def run_ours(args):
 
     # ---- CPU baseline: the oracle on a bounded sample of the same workload
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:   # rank 0 at N = 1 only
         import oracle
         threads = oracle.num_threads(0)
         # bounded sample: whole passes over the batch's query tokens until about 10 s of CPU work
@@ -402,6 +402,12 @@ def run_ours(args):
                "cores": min(threads, len(sample)), "kind": "oracle",
                "sample": "%d pass(es) over the batch's %d query tokens, full indexer+top-k+MLA in float64; "
                          "%.1f s wall on %s" % (passes, len(sample), wall_cpu, cpu_model())}
+        # and on one core: the query tokens of the first request
+        one = [int(t) for t in np.flatnonzero(w.token_req == w.token_req[0])]
+        t1 = oracle_sample(w, one, threads=1, shared=args.shared_sets)
+        cpu["single_thread"] = {"value": round(len(one) / t1, 3), "unit": "tokens/s",
+                                "sample": "the first request's %d query tokens on one thread; %.1f s wall"
+                                          % (len(one), t1)}
 
     line = {"metric": METRIC, "value": round(tokens / (ms_step * 1e-3), 1), "unit": "tokens/s", "n_gpus": world,
             "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
