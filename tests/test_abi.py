@@ -85,3 +85,55 @@ def test_calls_without_library_fail_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(hs, "_lib", None)
     with pytest.raises(hs.HSError):
         hs.load()
+
+
+_STRUCTS = {"hs_indexer_args": "_IndexerArgs", "hs_mla_args": "_MlaArgs", "hs_resolve_args": "_ResolveArgs",
+            "hs_kv_append_args": "_AppendArgs", "hs_kv_offload_args": "_OffloadArgs"}
+
+
+def _struct_fields(text, name):
+    """Field names of `typedef struct { ... } name;` in declaration order."""
+    m = re.search(r"typedef struct \{([^{}]*)\}\s*" + name + r"\s*;", text)
+    assert m, name
+    body = re.sub(r"/\*.*?\*/", "", m.group(1), flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        # "const int32_t* a, *b" / "int32_t T, H, k" -> names after the type
+        first, *rest = [d.strip() for d in decl.split(",")]
+        fields.append(re.findall(r"(\w+)\s*$", first)[0])
+        fields += [re.findall(r"(\w+)\s*$", r)[0] for r in rest]
+    return fields
+
+
+def test_argument_structs_match_the_binding(tmp_path):
+    """Every args struct of include/hs.h has the binding's field names, order, offsets and size
+    (offsets from the C compiler itself)."""
+    import subprocess
+    with open(os.path.join(ROOT, "include", "hs.h")) as f:
+        text = f.read()
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "hs.h"', "int main(void) {"]
+    fields = {}
+    for cname in _STRUCTS:
+        fields[cname] = _struct_fields(text, cname)
+        lines.append('printf("%s size %%zu\\n", sizeof(%s));' % (cname, cname))
+        for fld in fields[cname]:
+            lines.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (cname, fld, cname, fld))
+    lines += ["return 0;", "}"]
+    src, exe = tmp_path / "layout.c", tmp_path / "layout"
+    src.write_text("\n".join(lines) + "\n")
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {}
+    for ln in out:
+        if ln:
+            parts = ln.split()
+            got[(parts[0], parts[1])] = int(parts[2])
+    for cname, pyname in _STRUCTS.items():
+        cls = getattr(hs, pyname)
+        assert [f[0] for f in cls._fields_] == fields[cname], cname
+        assert ctypes.sizeof(cls) == got[(cname, "size")], cname
+        for fld in fields[cname]:
+            assert getattr(cls, fld).offset == got[(cname, fld)], (cname, fld)
