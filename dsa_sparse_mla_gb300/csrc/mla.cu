@@ -15,8 +15,8 @@
 //               per block), so QK starts on the first blocks while later ones are still being
 //               written; PV releases the stage pair by pair (one barrier per 128-dim M-tile),
 //               so the next tile's first blocks are written while PV still reads the last ones.
-//               Producers load and dequantise the next tile into registers while they wait for a
-//               free stage, so global-memory latency is off the MMA chain;
+//               Producers load the next tile into registers part by part as the current one is
+//               written, so global-memory latency is mostly off the MMA chain;
 //   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 64 rows,
 //               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile and an S
 //               buffer are ready;
@@ -194,7 +194,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Software pipeline per warp:
     //   tile i+4: index entries (lanes 0-7)     tile i+3: block-table entries
     //   tile i+2: rows prefetched into L2 by the TMA engine (one 656-byte bulk prefetch per row)
-    //   tile i+1: row data loaded into registers
+    //   tile i+1: row data loaded into registers, each part as soon as tile i's part in those
+    //             registers has been written (so most of the loads are in flight while the
+    //             rest of the stage is still being released)
     //   tile i  : dequantised into its stage, block by block, once the stage is free.
     // Loads are volatile so they are issued here and not next to their first use.
     const int sub = lane & 3;          // 16-byte piece of a 64-byte latent block
@@ -274,8 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!go && lane == 0) *abort_flag = 1;
       return go != 0;
     };
-    auto publish = [&](int i) -> bool {
+    auto publish = [&](int i, int64_t next_row) -> bool {
       const int s = i & 1;
+      // tile i+1's rows are loaded into the registers tile i's rows leave, as soon as each part
+      // has been written: the loads are in flight while the rest of the stage is released
+      const int64_t n0 = __shfl_sync(0xffffffffu, next_row, rlat);
+      const uint8_t* nsrc = p.kv + (n0 >= 0 ? n0 : 0) * HS_KV_ROW_BYTES + 16 * sub;
       if (!wait_empty(s, 0, i)) return false;
       uint8_t* st = sStage + s * kStageBytes;
       uint64_t* fb = full + s * kBlocks;
@@ -307,6 +313,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&fb[2 * g]);
           mbar_arrive(&fb[2 * g + 1]);
         }
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb)
+          lat[2 * g + bb] = n0 >= 0 ? ldg_nc_v4(nsrc + 64 * (2 * g + bb)) : make_uint4(0, 0, 0, 0);
+      }
+      if (lane < 8 && next_row >= 0) {
+        const uint4 v = ldg_nc_v4(p.kv + next_row * HS_KV_ROW_BYTES + HS_D_LATENT);
+        scl = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+      } else {
+        scl = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       // RoPE block (bf16 as stored); it held P of the tile before, released last
       if (!wait_empty(s, 4, i)) return false;
@@ -316,6 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&fb[8]);
+      {
+        const int64_t r1 = __shfl_sync(0xffffffffu, next_row, rrope);
+        const int64_t r2 = __shfl_sync(0xffffffffu, next_row, 4 + rrope);
+        rope[0] = r1 >= 0 ? ldg_nc_v4(p.kv + r1 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
+                          : make_uint4(0, 0, 0, 0);
+        rope[1] = r2 >= 0 ? ldg_nc_v4(p.kv + r2 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
+                          : make_uint4(0, 0, 0, 0);
+      }
       return true;
     };
     // prologue: tile 0 in registers, tile 1 prefetched into L2, tile 2 block entries and tile 3
@@ -338,11 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t bA = ld_blk(jA, rA);  // block-table entries travel with their index entries
     int32_t jB = ld_idx(rB);
     for (int i = 0; i < ntot; ++i) {
-      if (!publish(i)) break;
-      // advance: tile i+1 into registers (from L2), tile i+2 into L2, tile i+3 block entries,
-      // tile i+4 index entries
+      // publishes tile i and leaves tile i+1 in registers (from L2); then tile i+2 into L2,
+      // tile i+3 block entries, tile i+4 index entries
+      if (!publish(i, row_next)) break;
       my_row = row_next;
-      ld_rows(my_row);
       row_next = phys_row(jA, bA);
       if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
       jA = jB;
