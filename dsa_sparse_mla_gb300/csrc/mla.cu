@@ -9,7 +9,8 @@
 // One CTA per query token (416 threads):
 //   warps 0-7   gather 64 rows per tile (warp w owns rows 8w..8w+7; one 16-byte load per lane
 //               brings one 64-dim block of all 8 rows), dequantise latent = e4m3 * group scale to
-//               fp16 (exact e4m3 -> fp16 conversion, one rounding for the scale) and write it, with
+//               fp16 (exact e4m3 -> fp16 conversion, then code * scale rounded once to fp16 with
+//               the scale split into two fp16 parts; see dequant8_f16) and write it, with
 //               the bf16 RoPE part as stored, into a 128-byte-swizzled [dim block][row] tile
 //               (2 stages). Blocks are published in pairs as soon as they are written (a barrier
 //               per block), so QK starts on the first blocks while later ones are still being
@@ -20,7 +21,8 @@
 //   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 64 rows,
 //               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile and an S
 //               buffer are ready;
-//   warps 9-12  first convert Q's latent dims to fp16 in shared memory, then run the online
+//   warps 9-12  first convert Q's latent dims to fp16 in shared memory (a head's row whose largest
+//               value fp16 cannot hold at full precision is scaled by a power of two), then run the online
 //               softmax: two threads share each head's row of S (one shuffle for the max); P goes
 //               as fp16 into the stage's RoPE block, which QK no longer needs, so P is double
 //               buffered with the stages. The last of the four warps to finish a tile (a counter
@@ -59,20 +61,21 @@ constexpr int kOffStage = kQBytes;
 constexpr int kOffValid = kOffStage + 2 * kStageBytes;  // uint8 [2][64]
 constexpr int kOffAlpha = kOffValid + 128;          // float [64]
 constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
+constexpr int kOffQe = kOffInvL + 256;              // int [64]: per-head exponent e of the current query
 constexpr int kEmpty = 5;                 // per stage: 4 latent block pairs (one PV M-tile each) + RoPE/P
 constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 10;
-constexpr int kOffBar = kOffInvL + 256;
+constexpr int kOffBar = kOffQe + 256;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort, P counter
 constexpr int kSmem = kOffMisc + 16 + 1024;
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kF16Max = 65504.f;
 constexpr float kScaleMax = 65504.f / 448.f;     // |code * scale| stays finite in fp16
 constexpr float kScaleMin = 6.103515625e-05f;    // 2^-14: scales stay fp16 normals
 
 struct Params {
   int32_t T, H, k;
+  const __nv_bfloat16* q;  // [T][H][576], also loaded by TMA; read directly for the per-head maxima
   const uint8_t* kv;
   int64_t R;
   const int32_t* idx;
@@ -102,16 +105,21 @@ __host__ __device__ __forceinline__ int64_t unit_begin(int64_t c, int64_t U, int
 // CTA of a persistent launch holding unit u: the largest c with unit_begin(c) <= u.
 __device__ __forceinline__ int64_t unit_cta(int64_t u, int64_t U, int64_t C) { return ((u + 1) * C - 1) / U; }
 
-// 8 e4m3 codes (two 32-bit words) -> 8 fp16 values code * scale: the e4m3 -> fp16 conversion is
-// exact, the packed multiply rounds once.
-__device__ __forceinline__ uint4 dequant8_f16(uint32_t w0, uint32_t w1, uint32_t scale2) {
+// 8 e4m3 codes (two 32-bit words) -> 8 fp16 values code * scale, rounded once. The fp32 group
+// scale is split into fp16 parts hi + lo (hi = fp16(scale), lo = fp16(scale - hi)); the
+// e4m3 -> fp16 conversion is exact, t = code * lo is a correction of relative size 2^-11 whose own
+// rounding is ~2^-22 of the result, and fma(code, hi, t) rounds the sum once. Rounding the scale
+// to fp16 alone would give every value of a (row, group) the same relative error (up to 2^-11), a
+// bias that large logits turn into a coherent shift of that row's softmax weight.
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t w0, uint32_t w1, uint32_t hi2, uint32_t lo2) {
   uint4 r;
-  asm("{ .reg .b16 a, b, c, d; .reg .b32 x, y, z, u;\n"
+  asm("{ .reg .b16 a, b, c, d; .reg .b32 x, y, z, u, tx, ty, tz, tu;\n"
       " mov.b32 {a, b}, %4; mov.b32 {c, d}, %5;\n"
       " cvt.rn.f16x2.e4m3x2 x, a; cvt.rn.f16x2.e4m3x2 y, b; cvt.rn.f16x2.e4m3x2 z, c; cvt.rn.f16x2.e4m3x2 u, d;\n"
-      " mul.rn.f16x2 %0, x, %6; mul.rn.f16x2 %1, y, %6; mul.rn.f16x2 %2, z, %6; mul.rn.f16x2 %3, u, %6; }"
+      " mul.rn.f16x2 tx, x, %7; mul.rn.f16x2 ty, y, %7; mul.rn.f16x2 tz, z, %7; mul.rn.f16x2 tu, u, %7;\n"
+      " fma.rn.f16x2 %0, x, %6, tx; fma.rn.f16x2 %1, y, %6, ty; fma.rn.f16x2 %2, z, %6, tz; fma.rn.f16x2 %3, u, %6, tu; }"
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "r"(w0), "r"(w1), "r"(scale2));
+      : "r"(w0), "r"(w1), "r"(hi2), "r"(lo2));
   return r;
 }
 
@@ -133,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sValid = smem + kOffValid;
   float* sAlpha = (float*)(smem + kOffAlpha);
   float* sInvL = (float*)(smem + kOffInvL);
+  int32_t* sQe = (int32_t*)(smem + kOffQe);
   uint64_t* bars = (uint64_t*)(smem + kOffBar);
   uint64_t* full = bars + 0;                 // [2][9] producers wrote dim block b -> QK
   uint64_t* empty = bars + 2 * kBlocks;      // [2][5] PV done with block pair m (m = 4: RoPE/P) -> producers
@@ -294,14 +303,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sg = g == 0 ? scl.x : g == 1 ? scl.y : g == 2 ? scl.z : scl.w;
         const float scale = __shfl_sync(0xffffffffu, sg, rlat);
         range_ok &= scale == 0.f || (fabsf(scale) >= kScaleMin && fabsf(scale) <= kScaleMax);
-        const __half2 s2 = __float2half2_rn(scale);
-        const uint32_t s2u = *reinterpret_cast<const uint32_t*>(&s2);
+        const __half shi = __float2half_rn(scale);
+        const __half2 h2 = __half2half2(shi);
+        const __half2 l2 = __float2half2_rn(scale - __half2float(shi));  // scale - hi is exact in fp32
+        const uint32_t h2u = *reinterpret_cast<const uint32_t*>(&h2);
+        const uint32_t l2u = *reinterpret_cast<const uint32_t*>(&l2);
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int b = 2 * g + bb;
           const uint4 v = lat[b];
-          const uint4 lo = dequant8_f16(v.x, v.y, s2u);
-          const uint4 hi = dequant8_f16(v.z, v.w, s2u);
+          const uint4 lo = dequant8_f16(v.x, v.y, h2u, l2u);
+          const uint4 hi = dequant8_f16(v.z, v.w, h2u, l2u);
           uint8_t* blk = st + b * kBlk;
           *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * sub)) = lo;
           *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * sub + 16)) = hi;
@@ -450,32 +462,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t q = u / ntq;
       const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
       u = q * ntq + tb;
+      // Q's latent dims (blocks 0-7) bf16 -> fp16 in place. Chunk c = sm_tid + 128 j (16 bytes) is dim
+      // block j / 4 of head row (sm_tid / 8) + 16 (j % 4), so the 8 lanes sm_tid & ~7 .. + 7 hold all
+      // of a row's chunks and agree on its largest |q| with three shuffles. A row whose largest
+      // value lies outside [2^-6, 2^15) (rare: fp16 would overflow, or lose precision to its
+      // subnormal range) is then rewritten from global memory scaled by an exact power of two 2^e
+      // that puts its largest value in [2^14, 2^15), RoPE block included (bf16, exact); the softmax
+      // multiplies that head's logits by 2^-e. Other rows keep e = 0.
+      float sc_log2;  // softmax scale * log2(e) * 2^-e of this thread's head
       {
-        // Q's latent dims (blocks 0-7) bf16 -> fp16 in place; the RoPE block stays bf16
         const bool qok = warp_wait(q_full, (uint32_t)seg & 1u, p.err, lane);
-        bool in_range = true;
+        const int sm_tid = tid - (kThreads - kSmThreads);
+        bool finite = true;
         if (qok) {
+          uint32_t rmax[4] = {0u, 0u, 0u, 0u};  // packed maxima of |bf16| bit patterns (NaN above inf)
           uint4* q4 = reinterpret_cast<uint4*>(sQ);
-          const int sm_tid = tid - (kThreads - kSmThreads);
 #pragma unroll 4
-          for (int c = sm_tid; c < 8 * kBlk / 16; c += kSmThreads) {
+          for (int j = 0; j < 32; ++j) {
+            const int c = sm_tid + kSmThreads * j;
             uint4 v = q4[c];
             uint32_t* w = &v.x;
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu) {
+              rmax[j & 3] = __vmaxu2(rmax[j & 3], w[uu] & 0x7FFF7FFFu);
               const float lo = __uint_as_float(w[uu] << 16), hi = __uint_as_float(w[uu] & 0xFFFF0000u);
-              in_range &= fabsf(lo) < kF16Max && fabsf(hi) < kF16Max;
               const __half2 h2 = __floats2half2_rn(lo, hi);
               w[uu] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             q4[c] = v;
           }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) rmax[r] = __vmaxu2(rmax[r], __shfl_xor_sync(0xffffffffu, rmax[r], o));
+            const uint32_t amax = max(rmax[r] & 0xFFFFu, rmax[r] >> 16);
+            const int row = (sm_tid >> 3) + 16 * r;
+            finite &= amax < 0x7F80u || row >= p.H;
+            int e = 0;
+            if (amax >= 0x4700u && amax < 0x7F80u) e = 14 - ((int)(amax >> 7) - 127);  // >= 2^15
+            else if (amax >= 0x0080u && amax < 0x3C80u) e = 14 - ((int)(amax >> 7) - 127);  // normal, < 2^-6
+            else if (amax > 0u && amax < 0x0080u) e = 126;  // bf16 subnormals only
+            if (row >= p.H) e = 0;  // rows of the next query (or beyond the tensor): not computed here
+            e = e < -126 ? -126 : (e > 126 ? 126 : e);
+            if ((sm_tid & 7) == 0) sQe[row] = e;
+            if (e != 0) {
+              // rare: rewrite the row from global memory, 9 chunks per lane (lane & 7 = chunk column)
+              const float f = __uint_as_float((uint32_t)(e + 127) << 23);  // 2^e
+              const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + (q * p.H + row) * HS_D_QK * 2;
+#pragma unroll 1
+              for (int b = 0; b < 9; ++b) {
+                const int chunk = sm_tid & 7;
+                uint4 v = ldg_nc_v4(src + b * 128 + 16 * chunk);
+                uint32_t* w = &v.x;
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu) {
+                  const float lo = __uint_as_float(w[uu] << 16) * f, hi = __uint_as_float(w[uu] & 0xFFFF0000u) * f;
+                  if (b < 8) {
+                    const __half2 h2 = __floats2half2_rn(lo, hi);
+                    w[uu] = *reinterpret_cast<const uint32_t*>(&h2);
+                  } else {
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                    w[uu] = *reinterpret_cast<const uint32_t*>(&b2);
+                  }
+                }
+                *reinterpret_cast<uint4*>(sQ + b * kBlk + sw128_offset(row, 16 * chunk)) = v;
+              }
+            }
+          }
         }
-        if (!in_range) flag_error(p.err, HS_FLAG_RANGE);
+        if (!finite) flag_error(p.err, HS_FLAG_RANGE);
         if (!qok) *abort_flag = 1;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
+        named_bar(1, kSmThreads);  // every row's exponent written (QK has already been released)
+        sc_log2 = p.scale_log2 * __uint_as_float((uint32_t)(127 - sQe[h]) << 23);
       }
       float m_ref = -INFINITY, l_part = 0.f;
 #pragma unroll 1
@@ -510,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 16; ++c) {
               const int col = q4 * 16 + c;
               const bool valid = (w4[c >> 2] >> (8 * (c & 3))) & 0xFFu;
-              const float v = valid ? __uint_as_float(xr[col]) * p.scale_log2 : -INFINITY;
+              const float v = valid ? __uint_as_float(xr[col]) * sc_log2 : -INFINITY;
               xr[col] = __float_as_uint(v);
               mt = fmaxf(mt, v);
             }
@@ -775,6 +836,7 @@ cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const
   p.T = a->T;
   p.H = a->H;
   p.k = a->k;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(a->q);
   p.kv = a->kv_pool;
   p.R = a->R;
   p.idx = a->idx;

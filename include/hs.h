@@ -178,9 +178,12 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  *
  * Compute precision: the latent part of q and the dequantised latent rows enter the tensor cores as
  * IEEE half (fp16, 10-bit mantissa), the RoPE part as bf16, P as fp16, all accumulated in fp32.
- * fp16 bounds the inputs: |q| < 65504 on the latent dims and group scales in [2^-14, 146]
- * (so |code * scale| < 65504). A value outside these bounds sets HS_FLAG_RANGE; the result is then
- * not reliable.
+ * Each dequantised value code * scale is rounded once to fp16. A head's q row whose largest |q|
+ * lies outside [2^-6, 2^15) is scaled by an exact power of two that puts that value in
+ * [2^14, 2^15) before the fp16 conversion (its logits are scaled back in fp32), so any finite bf16
+ * q is accepted at full fp16 precision. fp16 bounds the group scales to [2^-14, 146] (so
+ * |code * scale| < 65504). A scale outside these bounds, or a latent q value that is not finite,
+ * sets HS_FLAG_RANGE; the result is then not reliable.
  *
  * idx entries < 0 are padding and skipped. With block_table == NULL they are physical pool rows
  * (< R); otherwise logical token indices of request token_req[t] mapped through the paged layout.

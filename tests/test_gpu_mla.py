@@ -104,16 +104,49 @@ def test_workspace_too_small_rejected():
         hs_sparse_mla_fwd(q, kvt, it, 0.1, out, err, workspace=ws)
 
 
-def test_distinct_group_scales_and_large_logits():
+@pytest.mark.parametrize("sigma", [1.5, 3.0, 4.0])
+def test_distinct_group_scales_and_large_logits(sigma):
+    """Four different group scales per row (up to 7x the row's amax / 448) and a peaky softmax:
+    with q ~ N(0, 3^2) the logits' spread is a few tens, so a few rows carry the weight and any
+    bias in a row's dequantised values moves the output."""
     n, T, H, k = 600, 5, 64, 512
     kv = _rows(n, seed=3, group_scales=True)
-    q = inputs.bf16_bits(inputs.Stream(4).sub("q").normal((T, H, 576), sigma=1.5))  # peaky softmax (logit std ~4.5)
+    q = inputs.bf16_bits(inputs.Stream(4).sub("q").normal((T, H, 576), sigma=sigma))
     rng = np.random.default_rng(0)
     idx = np.stack([rng.permutation(n)[:k] for _ in range(T)]).astype(np.int32)
     out, lse, flag = _run(q, kv, idx, 0.125)
     assert flag == 0
     ref, lref = oracle.sparse_mla(q, kv, idx, 0.125)
     check_mla(out, lse, ref, lref)
+
+
+@pytest.mark.parametrize("sigma", [1e-5, 1e-30, 3e4, 1e12])
+def test_query_magnitudes_outside_fp16(sigma):
+    """Queries far below fp16's normal range (|q| < 2^-14) or far above its largest value: every
+    head's row is brought into fp16's range by an exact power of two, so the result matches the
+    oracle as for ordinary magnitudes and no range flag is raised. The softmax scale keeps the
+    logits of order one; one head is scaled 2^20 above the others."""
+    n, T, H, k = 700, 4, 64, 600
+    kv = _rows(n, seed=8)
+    x = inputs.Stream(9).sub("q").normal((T, H, 576))
+    x[:, 5] *= 2.0 ** 20
+    q = inputs.bf16_bits(x * sigma)
+    rng = np.random.default_rng(2)
+    idx = np.stack([rng.permutation(n)[:k] for _ in range(T)]).astype(np.int32)
+    scale = 0.3 / sigma
+    out, lse, flag = _run(q, kv, idx, scale)
+    assert flag == 0
+    ref, lref = oracle.sparse_mla(q, kv, idx, scale)
+    check_mla(out, lse, ref, lref)
+
+
+def test_non_finite_query_is_flagged():
+    kv = _rows(64, seed=6)
+    x = inputs.Stream(6).sub("q").normal((2, 8, 576))
+    x[1, 3, 100] = np.inf
+    q = inputs.bf16_bits(x)
+    _, _, flag = _run(q, kv, np.arange(64, dtype=np.int32)[None].repeat(2, 0), 0.05)
+    assert flag & 0x40
 
 
 def test_paged_logical_indices():
