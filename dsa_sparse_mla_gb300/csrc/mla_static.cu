@@ -18,7 +18,10 @@
 //    streams, or two host threads) race on it; a caller must order them.
 //  - The host needs the array's device address, which is not the address of the host-side symbol.
 //    The first call on each device looks it up with cudaGetSymbolAddress while that device is
-//    current and caches it; make that first call before capturing a stream.
+//    current and caches it; make that first call before capturing a stream. The cache is keyed
+//    by device ordinal for the life of the process: after cudaDeviceReset, or from a different
+//    driver context on the same device, the cached address is stale, so this entry point must not
+//    be used in a process that does either.
 #include <mutex>
 
 #include "common.cuh"

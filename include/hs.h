@@ -255,7 +255,9 @@ hs_status hs_sparse_mla_workspace_size(int32_t H, uint64_t* bytes);
  *  - HS_ERR_UNSUPPORTED when the split path would need more than those 24 MiB (H heads on a
  *    device with so many SMs that 2 * SMs * H * 1028 bytes exceed them).
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *    with that device current; make it before capturing a stream.
+ *    with that device current; make it before capturing a stream. The address is cached per
+ *    device ordinal for the life of the process, so the call must not be used after
+ *    cudaDeviceReset or from a second driver context on the same device.
  *  - All calls share the array and it keeps the last call's contents; nothing in it needs to
  *    start at zero. Calls that overlap on the GPU race on it and must be ordered by the caller. */
 hs_status hs_sparse_mla_fwd_static(const hs_mla_args* a, hs_stream_t stream);

@@ -1,6 +1,6 @@
 """End-to-end parity of one hot-path step (indexer -> top-k -> sparse MLA) on the benchmark's
-workloads: the tiny prefill in full, and the MTP-decode and chunked-prefill workloads at full
-size on sampled query tokens (the oracle computes those tokens one by one)."""
+workloads: the tiny prefill in full, and the MTP-decode, chunked-prefill and long-prefill
+workloads at full size on sampled query tokens (the oracle computes those tokens one by one)."""
 import numpy as np
 import pytest
 
@@ -47,11 +47,27 @@ def test_mtp_decode_full_size_sampled():
 
 
 def test_chunked_prefill_full_size_sampled():
+    """The 2048-token chunk after 65,536 cached tokens: 16 tokens spread over the chunk, so that
+    the persistent indexer's and the MLA's per-position work splits are sampled throughout."""
     w = inputs.config3()
     hp = HotPath(DeviceWorkload.from_host(w))
     hp.step()
     assert hs_check_flag(hp.err) == 0
-    _check_tokens(w, hp, [0, 777, 2047])
+    rows = np.unique(np.concatenate([np.linspace(0, w.T - 1, 14).round().astype(int), [1, 1000]]))
+    assert len(rows) == 16
+    _check_tokens(w, hp, rows)
+
+
+@pytest.mark.parametrize("chunk", [31, 63])
+def test_long_prefill_full_size_sampled(chunk):
+    """Long prefill of one 131,072-token sequence in 64 chunks of 2048: a middle chunk and the
+    last one (each query sees up to 131,072 keys), whole-chunk launches, sampled tokens."""
+    w = inputs.config4(chunk)
+    hp = HotPath(DeviceWorkload.from_host(w))
+    hp.step()
+    assert hs_check_flag(hp.err) == 0
+    assert int(w.token_kvlen.max()) == (chunk + 1) * 2048
+    _check_tokens(w, hp, [0, 1023, 2047])
 
 
 def test_repeat_is_deterministic():

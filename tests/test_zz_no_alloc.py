@@ -45,13 +45,23 @@ def _static_call(q, kv, idx, scale, out, lse, err):
 def test_static_scratch_matches_workspace_call_twice():
     torch.cuda.set_device(0)
     H, k, n, scale = 64, 2048, 6000, 1 / math.sqrt(576)
-    # 40 queries on a many-SM GPU: the split-work path (and so the scratch) is taken
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     for call, (T, seed) in enumerate([(40, 101), (37, 202)]):
+        # fewer queries than 3/4 of one wave: the split-work path, and so the scratch, is taken
+        assert 4 * T < 3 * sms, "this device has too few SMs for the split path at T = %d" % T
         q, kv, idx = _inputs(T, H, k, n, seed)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         out_s = torch.full((T, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
         lse_s = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
         _static_call(q, kv, idx, scale, out_s, lse_s, err)
+        torch.cuda.synchronize()
+        # nothing allocated: not through torch, and (after the first call, which may load the
+        # library's device code and its static array) not on the device at all
+        assert torch.cuda.memory_allocated() == alloc0
+        if call > 0:
+            assert torch.cuda.mem_get_info()[0] == free0
         out_w = torch.empty_like(out_s)
         lse_w = torch.empty_like(lse_s)
         ws = torch.empty(hs_sparse_mla_workspace_size(H), dtype=torch.uint8, device="cuda")
