@@ -1,21 +1,23 @@
 """Benchmark of the sparse-MLA layer hot path on one GB300 (or N, one process per GPU).
 
 One step = one pass of the whole hot path over one batch: hs_indexer_scores -> hs_topk ->
-hs_sparse_mla_fwd, on the MTP-decode batch (64 requests x (1+3) query tokens, contexts
-16K-64K, 64 x 128-d FP8 index heads, top-2048, 64 MLA heads, paged FP8 KV). Prints one JSON
-line. Other workloads (tiny prefill, chunked prefill, long prefill chunks, HiSparse decode) are
-available with --config for analysis; the default line is the MTP-decode one.
+hs_sparse_mla_fwd. The default line is the long prefill: one step is one 131,072-token sequence
+as 64 sequential chunks of 2,048 tokens (64 x 128-d FP8 index heads, top-2048, 64 MLA heads,
+paged FP8 KV), i.e. 192 launches; it also reports the per-chunk curve, the chunk where the indexer
+overtakes attention, and the MTP-decode (64 requests x (1+3) tokens, contexts 16K-64K) and
+chunked-prefill (2,048 tokens after 65,536) workloads as extra keys. Other workloads are available
+for analysis with --config 1|2|3|5, --kv-append, --kv-offload.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 4]
 
 Timing: W untimed steps, then K steps; before each timed step a 256 MB buffer is written so L2
-(126 MB) holds nothing of the previous step; each step is bracketed by CUDA events on the
-launching stream; the reported time is the mean per step, max over ranks. Per-kernel events
-inside the timed steps give each kernel's average duration for the roofline. `e2e` repeats the
-step through the same API with the step's inputs copied from pinned host memory and the outputs
-copied back inside the timed region. `cpu_baseline` times the CPU oracle (test
-infrastructure, never on the product path) on a bounded sample of the same workload.
-`--impl reference` times only that oracle, which is the reference implementation here.
+(126 MB) holds nothing of the previous step; launches are bracketed by CUDA events on the
+launching stream; the reported time is the mean per step, max over ranks. Per-kernel events give
+each kernel's duration for the roofline. `e2e` repeats the step through the same API with the
+step's inputs copied from pinned host memory and the outputs copied back inside the timed region.
+`cpu_baseline` times the CPU oracle (test infrastructure, never on the product path) on a bounded
+sample of the same workload. `--impl reference` times only that oracle, which is the reference
+implementation here.
 """
 from __future__ import annotations
 
@@ -433,6 +435,111 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------------ peaks ---------------
+
+def measure_fp8_peak(seconds: float = 3.0):
+    """Dense e4m3 GEMM rate of this GPU through cuBLASLt (torch._scaled_mm, 8192^3, unit scales,
+    bf16 output, 2 n^3 FLOPs): the best of 10 launches (burst) and launches back to back for about
+    `seconds` (sustained, under the power cap). None if the call is unavailable."""
+    import torch
+    n = 8192
+    try:
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn).t()   # column-major B
+        one = torch.ones((), dtype=torch.float32, device="cuda")
+        f = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+    except (RuntimeError, AttributeError, TypeError) as e:  # pragma: no cover - depends on the build
+        return {"error": str(e).splitlines()[0][:200]}
+    flop = 2.0 * n ** 3
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        f()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    count = 0
+    t0 = time.perf_counter()
+    e0.record()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(10):
+            f()
+        count += 10
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    del a, b
+    return {"fp8_tflops": round(flop / (best * 1e-3) / 1e12, 1),
+            "fp8_tflops_sustained": round(flop * count / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
+            "how": "torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3 (2 n^3 FLOPs): best of 10 (burst) and "
+                   "%d launches back to back (sustained)" % count}
+
+
+def kernel_rooflines(works, ms, hbm, fp8, bf16):
+    """Per kernel: algorithmic bytes and FLOPs summed over `works` (one dict of costmodel Work per
+    launch group), measured ms (summed likewise), roofline ms (per launch the slower of bytes at
+    HBM bandwidth and FLOPs at the kernel's tensor peak, summed) and the bound that dominates."""
+    out = {}
+    for name in ("indexer", "topk", "mla"):
+        peak = fp8 if name == "indexer" else bf16
+        b = sum(w[name].bytes for w in works)
+        fl = sum(w[name].flops for w in works)
+        t_bytes = sum(w[name].bytes / (hbm * 1e9) for w in works)
+        t_flops = sum(w[name].flops / (peak * 1e12) for w in works)
+        t_roof = sum(max(w[name].bytes / (hbm * 1e9), w[name].flops / (peak * 1e12)) for w in works)
+        t = ms[name] * 1e-3
+        out[name] = {"ms": round(ms[name], 4), "bytes": b, "flops": fl, "gbs": round(b / t / 1e9, 1),
+                     "tflops": round(fl / t / 1e12, 1), "roofline_ms": round(t_roof * 1e3, 4),
+                     "roofline_frac": round(t_roof / t, 4), "bound": "hbm" if t_bytes >= t_flops else "tensor"}
+    tot = sum(ms.values())
+    for name in out:
+        out[name]["share"] = round(ms[name] / tot, 4)
+    return out
+
+
+def measure_hot_path(w, steps: int, warmup: int, dev, peaks):
+    """One workload's step (indexer -> top-k -> sparse MLA on all its query tokens): mean time per
+    step and per kernel over `steps` timed steps, a 256 MB L2 flush before each."""
+    import torch
+    import dsa_sparse_mla_gb300 as hs
+    from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
+    hp = HotPath(DeviceWorkload.from_host(w, dev))
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        hp.step()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        e = ev[i]
+        e[0].record(stream)
+        hp.indexer()
+        e[1].record(stream)
+        hp.topk()
+        e[2].record(stream)
+        hp.mla()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    ms = {n: float(np.mean([ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps)]))
+          for j, n in enumerate(("indexer", "topk", "mla"))}
+    step_ms = float(np.mean([ev[i][0].elapsed_time(ev[i][3]) for i in range(steps)]))
+    kern = kernel_rooflines([work_of(w)], ms, peaks["hbm"], peaks["fp8"], peaks["bf16"])
+    flag = hs.hs_check_flag(hp.err)
+    del hp, flush
+    torch.cuda.empty_cache()
+    return {"value": round(w.T / (step_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(step_ms, 4),
+            "steps": steps, "query_tokens": w.T, "kernels": kern,
+            "layer_roofline_frac": round(sum(k["roofline_ms"] for k in kern.values()) / sum(ms.values()), 4),
+            "device_flag": flag}
+
+
 # ------------------------------------------------------------------------ analysis modes ----
 
 def _timed(fn, flush, reps):
@@ -450,47 +557,231 @@ def _timed(fn, flush, reps):
     return float(statistics.median(a.elapsed_time(b) for a, b in ev))
 
 
-def run_long_prefill(args):
-    """Long prefill from scratch: 131,072 tokens as 64 sequential chunks of 2,048. The cache holds
-    the whole sequence; chunk c's queries are positions 2048 c .. 2048 c + 2047 (their values are
-    the same draws for every chunk, only their positions move). Per chunk: indexer, top-k and sparse
-    MLA times; the indexer-overtakes-attention chunk is reported."""
+def long_prefill_cpu_sample(chunks, threads=0):
+    """The CPU oracle on a stratified sample of the long-prefill pass: 16 query tokens evenly spaced
+    in each of 8 evenly spaced chunks (3, 11, ..., 59), so that the sampled positions' mean cost is
+    the pass's mean cost per token. Returns (tokens, wall seconds)."""
+    picks = [c for c in range(3, len(chunks), 8)]
+    tok = np.linspace(0, chunks[0].T - 1, 16).round().astype(int).tolist()
+    wall = 0.0
+    for c in picks:
+        wall += oracle_sample(chunks[c], tok, threads=threads)
+    return len(picks) * len(tok), wall
+
+
+def run_long_prefill_pass(args):
+    """The benchmark line: one step is one long-prefill pass, 131,072 tokens of one sequence as 64
+    sequential chunks of 2,048, each chunk through hs_indexer_scores -> hs_topk ->
+    hs_sparse_mla_fwd (192 launches). The cache and every chunk's query inputs are resident in
+    HBM when the timed region starts; each chunk's queries see every earlier token and themselves.
+    Reports whole-pass tokens/s, the per-chunk time curve with the chunk at which the indexer
+    overtakes attention, the roofline of the dominant kernel over the pass, the MTP-decode and
+    chunked-prefill workloads as extra keys, e2e through host buffers and the CPU oracle."""
+    import dataclasses
     import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
     import dsa_sparse_mla_gb300 as hs
-    from dsa_sparse_mla_gb300 import costmodel as cm, inputs
-    from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
-    torch.cuda.set_device(0)
+    from dsa_sparse_mla_gb300 import inputs
+    from dsa_sparse_mla_gb300.pipeline import LongPrefillPass
+
     hs.load()
-    w = inputs.config4(0)
-    nchunks, clen = 64, 2048
-    w.token_kvlen = (np.arange(clen, dtype=np.int32) + (nchunks - 1) * clen + 1)  # ld for the last chunk
-    dw = DeviceWorkload.from_host(w)
-    hp = HotPath(dw)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    chunks = list(range(0, nchunks, max(1, args.chunk_stride)))
-    if chunks[-1] != nchunks - 1:
-        chunks.append(nchunks - 1)
-    curve = []
-    for c in chunks:
-        kv = np.arange(clen, dtype=np.int32) + c * clen + 1
-        dw.token_kvlen.copy_(torch.from_numpy(kv))
-        w.token_kvlen = kv
-        wk = work_of(w)
-        t_i = _timed(hp.indexer, flush, args.reps)
-        t_k = _timed(hp.topk, flush, args.reps)
-        t_m = _timed(hp.mla, flush, args.reps)
-        curve.append({"chunk": c, "ctx_end": int((c + 1) * clen), "indexer_ms": round(t_i, 4), "topk_ms": round(t_k, 4),
-                      "mla_ms": round(t_m, 4), "indexer_tflops": round(wk["indexer"].flops / (t_i * 1e9), 1)})
-    flag = hs.hs_check_flag(hp.err)
+    peaks, peaks_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    bf16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
+    fp8m = measure_fp8_peak() if rank == 0 else None
+    if fp8m and "fp8_tflops_sustained" in fp8m:
+        fp8, fp8_src = fp8m["fp8_tflops_sustained"], "measured in this run (sustained e4m3 GEMM)"
+    else:
+        fp8, fp8_src = bf16 * FP8_PER_BF16, "derived: sustained bf16 x 2 (no e4m3 GEMM available)"
+    pk = {"hbm": hbm, "fp8": fp8, "bf16": bf16}
+
+    t0 = time.perf_counter()
+    chunks = inputs.config4_pass(seed=rank_seed(4, rank))
+    gen_s = time.perf_counter() - t0
+    n, T = len(chunks), chunks[0].T
+    total_tokens = n * T
+    lp = LongPrefillPass(chunks, dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    works = [work_of(w) for w in chunks]
+
+    for _ in range(args.warmup):
+        lp.step()
+    torch.cuda.synchronize()
+    if hs.hs_check_flag(lp.err):
+        raise SystemExit("device error flag set during warm-up: 0x%x" % hs.hs_check_flag(lp.err))
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(1 + 3 * n)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e = ev[i]
+        e[0].record(stream)
+        for c in range(n):
+            lp.indexer(c)
+            e[1 + 3 * c].record(stream)
+            lp.topk(c)
+            e[2 + 3 * c].record(stream)
+            lp.mla(c)
+            e[3 + 3 * c].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    t_pass = [ev[i][0].elapsed_time(ev[i][3 * n]) for i in range(K)]
+    per = np.array([[[ev[i][3 * c + j].elapsed_time(ev[i][3 * c + j + 1]) for j in range(3)] for c in range(n)]
+                    for i in range(K)]).mean(axis=0)          # [chunk, kernel] ms
+    ms_step = max_over_ranks(float(np.mean(t_pass)), world, dev)
+    flag = hs.hs_check_flag(lp.err)
+
+    # ---- end to end: every chunk's query inputs copied in from pinned host memory and its output
+    # and LSE copied back, chunk by chunk, on two copy streams (in, out) with two device buffer
+    # sets, so chunk c + 1's inputs and chunk c - 1's outputs move while chunk c computes
+    h_in = [[t.cpu().pin_memory() for t in lp.step_inputs(c)] for c in range(n)]
+    h_out = [(torch.empty_like(lp.out[c], device="cpu").pin_memory(),
+              torch.empty_like(lp.lse[c], device="cpu").pin_memory()) for c in range(n)]
+    d_in = [[torch.empty_like(t) for t in lp.step_inputs(0)] for _ in range(2)]
+    d_out = [(torch.empty_like(lp.out[0]), torch.empty_like(lp.lse[0])) for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for row in h_in for t in row)
+    d2h = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in h_out)
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+
+    def copy_in(c):
+        st = c & 1
+        with torch.cuda.stream(cin):
+            if c >= 2:
+                cin.wait_event(done[st])          # chunk c - 2 has finished reading this set
+            for dst, h in zip(d_in[st], h_in[c]):
+                dst.copy_(h, non_blocking=True)
+            in_ready[st].record(cin)
+
+    def copy_out(c):
+        st = c & 1
+        with torch.cuda.stream(cout):
+            cout.wait_event(done[st])
+            h_out[c][0].copy_(d_out[st][0], non_blocking=True)
+            h_out[c][1].copy_(d_out[st][1], non_blocking=True)
+            out_done[st].record(cout)
+
+    e2e_t = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    barrier(world)
+    torch.cuda.synchronize()
+    e2e_t[0].record(stream)
+    cin.wait_event(e2e_t[0])
+    copy_in(0)
+    for c in range(n):
+        st = c & 1
+        if c + 1 < n:
+            copy_in(c + 1)
+        stream.wait_event(in_ready[st])
+        if c >= 2:
+            stream.wait_event(out_done[st])       # chunk c - 2's outputs are on the host
+        q_idx, q_scale, weights, q_mla, kvlen = d_in[st]
+        lp.indexer(c, q_idx=q_idx, q_scale=q_scale, weights=weights, token_kvlen=kvlen)
+        lp.topk(c, token_kvlen=kvlen)
+        lp.mla(c, q_mla=q_mla, out=d_out[st][0], lse=d_out[st][1])
+        done[st].record(stream)
+        copy_out(c)
+    stream.wait_event(out_done[0])
+    stream.wait_event(out_done[1])
+    e2e_t[1].record(stream)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out[n - 1][0].view(torch.int16), lp.out[n - 1].cpu().view(torch.int16)), "e2e outputs differ"
+    ms_e2e = max_over_ranks(e2e_t[0].elapsed_time(e2e_t[1]), world, dev)
+    clk = clocks.stop() if rank == 0 else None
+    del h_in, h_out, d_in, d_out
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    ms = {name: float(per[:, j].sum()) for j, name in enumerate(("indexer", "topk", "mla"))}
+    kern = kernel_rooflines(works, ms, hbm, fp8, bf16)
+    dom = max(ms, key=ms.get)
+    kd = kern[dom]
+    if kd["bound"] == "hbm":
+        roof = {"bound": "hbm", "achieved": kd["gbs"], "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": kd["tflops"], "peak": fp8 if dom == "indexer" else bf16,
+                "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["kernel"] = dom
+    roof["achieved_over"] = "the kernel's 64 launches of one pass: algorithmic work / summed launch time"
+    roof["peak_source"] = ("HBM and bf16 %s (MEASURED_PEAKS.json); e4m3 %s" % (peaks_kind, fp8_src))
+    tr = recorded_traffic(dom, "long-prefill-chunk63")
+    roof["traffic"] = tr
+    if tr is not None:
+        roof["traffic_launch"] = "chunk 63 (2048 queries over up to 131,072 keys), one launch"
+        roof["algorithmic_bytes_launch"] = works[-1][dom].bytes
+    curve = [{"chunk": c, "ctx_end": int((c + 1) * T), "indexer_ms": round(float(per[c, 0]), 4),
+              "topk_ms": round(float(per[c, 1]), 4), "mla_ms": round(float(per[c, 2]), 4),
+              "indexer_tflops": round(works[c]["indexer"].flops / (per[c, 0] * 1e9), 1),
+              "mla_gbs": round(works[c]["mla"].bytes / (per[c, 2] * 1e6), 1)} for c in range(n)]
     cross = next((e["chunk"] for e in curve if e["indexer_ms"] > e["mla_ms"]), None)
-    total_ms = sum(e["indexer_ms"] + e["topk_ms"] + e["mla_ms"] for e in curve)
-    line = {"metric": "long-prefill per-chunk time curve (indexer+top-k+attn)", "workload": "long-prefill-128K",
-            "chunks_timed": len(curve), "chunk_tokens": clen, "curve": curve,
-            "indexer_overtakes_attention_at_chunk": cross,
-            "crossover_ctx_tokens": None if cross is None else (cross + 1) * clen,
-            "tokens_per_s_timed_chunks": round(len(curve) * clen / (total_ms * 1e-3), 1), "device_flag": flag,
-            "reps_per_kernel": args.reps, "l2": "256 MB write before each timed launch", "data": "synthetic"}
+
+    # ---- the other workloads of the same hot path, measured in the same run
+    others = {}
+    if not args.no_extra:
+        for cfg, steps in ((2, 200), (3, 20)):
+            w = build_workload(cfg, rank_seed(cfg, 0))
+            others[w.name] = measure_hot_path(w, steps, 3, dev, pk)
+            del w
+
+    # ---- CPU baseline: the oracle on a stratified sample of the pass
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        import oracle
+        threads = oracle.num_threads(0)
+        ntok, wall_cpu = long_prefill_cpu_sample(chunks)
+        cpu = {"value": round(ntok / wall_cpu, 3), "unit": "tokens/s", "cores": min(threads, 16), "kind": "oracle",
+               "sample": "16 query tokens evenly spaced in each of chunks 3, 11, ..., 59 of the pass (%d tokens, "
+                         "their mean cost is the pass's), full indexer+top-k+MLA in float64; %.1f s wall on %s"
+                         % (ntok, wall_cpu, cpu_model())}
+
+    line = {"metric": METRIC, "value": round(total_tokens * world / (ms_step * 1e-3), 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16",
+            "data": "synthetic",
+            "config": {"workload": "long-prefill-128K", "sequence_tokens": total_tokens, "chunks": n,
+                       "chunk_tokens": T, "index_heads": chunks[0].Hi, "index_dim": chunks[0].Di,
+                       "topk": chunks[0].topk, "mla_heads": chunks[0].H, "page": 64,
+                       "step": "one whole pass: 64 chunks x (indexer, top-k, sparse MLA)",
+                       "l2": "256 MB write before each timed pass (each pass reads 10.8 GB of query inputs)",
+                       "parallelism": "dp%d" % world},
+            "roofline": roof,
+            "layer_roofline_frac": round(sum(k["roofline_ms"] for k in kern.values()) / sum(ms.values()), 4),
+            "kernels": kern,
+            "peaks": dict(fp8m or {}, hbm_gbs=hbm, bf16_tflops_sustained=bf16),
+            "chunk_curve": curve, "indexer_overtakes_attention_at_chunk": cross,
+            "crossover_ctx_tokens": None if cross is None else (cross + 1) * T,
+            "other_workloads": others,
+            "e2e": {"value": round(total_tokens * world / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4), "steps": 1,
+                    "overlap": "chunk c+1's inputs in and chunk c-1's outputs out on two copy streams while chunk c "
+                               "computes (two device buffer sets)"},
+            "gpu_launches": 3 * n * K, "cpu_baseline": cpu, "clocks": clk, "wall_s_timed_region": round(wall, 3),
+            "inputs_generated_s": round(gen_s, 1), "device_flag": flag}
     print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 def run_kv_append(args):
@@ -634,26 +925,36 @@ def run_hisparse(args):
 # ------------------------------------------------------------------------ reference arm -----
 
 def run_reference(args):
-    """The CPU oracle timed as the reference implementation, on the same workload and metric."""
+    """The CPU oracle timed as the reference implementation, on the same workload and metric. On
+    the long-prefill pass a step is 16 query tokens evenly spaced in one chunk, the chunks cycling
+    through 3, 11, ..., 59 (their mean cost per token is the pass's); on the other workloads a
+    step is one query token per core."""
     rank, world, local = dist_info()
     if rank != 0:
         return
     import oracle
+    from dsa_sparse_mla_gb300 import inputs
     oracle.build()
     threads = oracle.num_threads(0)
-    w = build_workload(args.config, rank_seed(args.config, 0), args.requests)
-    per_step = max(4, threads)              # query tokens per step: one token per core
+    if args.config == 4:
+        picks = list(range(3, 64, 8))
+        ws = inputs.config4_pass(seed=rank_seed(4, 0), chunks=picks)
+        tok = np.linspace(0, ws[0].T - 1, 16).round().astype(int).tolist()
+        plan = [(ws[i % len(ws)], tok) for i in range(len(ws))]
+        name = "long-prefill-128K"
+    else:
+        w = build_workload(args.config, rank_seed(args.config, 0), args.requests)
+        per_step = max(4, threads)
+        plan = [(w, [(i * per_step + j) % w.T for j in range(per_step)]) for i in range(max(1, w.T // per_step))]
+        name = w.name
     # size the sample so that warm-up + timed steps stay within about three minutes
-    probe = oracle_sample(w, list(range(per_step)), threads=0)
+    probe = oracle_sample(plan[0][0], plan[0][1], threads=0)
     budget = 180.0
     steps_timed = max(1, min(args.steps, int(budget / max(probe, 1e-3)) - args.warmup))
-    for i in range(min(args.warmup, 1)):
-        oracle_sample(w, list(range(per_step)), threads=0)
     t = 0.0
     ntok = 0
     for i in range(steps_timed):
-        start = (i * per_step) % w.T
-        toks = [(start + j) % w.T for j in range(per_step)]
+        w, toks = plan[i % len(plan)]
         t += oracle_sample(w, toks, threads=0)
         ntok += len(toks)
     value = ntok / t
@@ -661,10 +962,11 @@ def run_reference(args):
             "steps": args.steps, "steps_timed": steps_timed, "warmup": args.warmup,
             "ms_per_step": round(1e3 * t / steps_timed, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "query_tokens_per_step": per_step},
+            "config": {"workload": name, "query_tokens_per_step": len(plan[0][1])},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle", "cores": threads,
                              "sample": "%d query tokens per step (indexer+top-k+MLA, float64) of %s, %d timed steps "
-                                       "on %s" % (per_step, w.name, steps_timed, cpu_model())},
+                                       "(the probe step untimed) on %s" % (len(plan[0][1]), name, steps_timed,
+                                                                           cpu_model())},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -672,14 +974,16 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 5 long-prefill passes, else 1000)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4,
+                    help="4 (default): the long-prefill pass; 1, 2, 3: one step of that workload; 5: HiSparse decode")
     ap.add_argument("--requests", type=int, default=64, help="decode batch size (profiling runs use fewer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--chunk-stride", type=int, default=1, help="--config 4: time every n-th chunk")
-    ap.add_argument("--reps", type=int, default=5, help="--config 4: timed launches per kernel and chunk")
+    ap.add_argument("--no-extra", action="store_true", help="--config 4: skip the MTP-decode and chunked-prefill keys")
+    ap.add_argument("--reps", type=int, default=5, help="--kv-append / --kv-offload: timed launches")
     ap.add_argument("--hisparse-steps", type=int, default=50, help="--config 5: decode steps")
     ap.add_argument("--kv-append", type=int, default=0, help="time hs_kv_append on this many new tokens instead")
     ap.add_argument("--kv-offload", type=int, default=0, help="time hs_kv_offload on about this many pages instead")
@@ -688,6 +992,8 @@ def main(argv=None):
                          "run for final tokens only)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.steps is None:
+        args.steps = 5 if (args.config == 4 and args.impl == "ours") else 1000
     if args.impl == "reference":
         run_reference(args)
     elif args.kv_append > 0:
@@ -695,7 +1001,7 @@ def main(argv=None):
     elif args.kv_offload > 0:
         run_kv_offload(args)
     elif args.config == 4:
-        run_long_prefill(args)
+        run_long_prefill_pass(args)
     elif args.config == 5:
         run_hisparse(args)
     else:

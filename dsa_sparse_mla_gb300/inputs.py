@@ -205,10 +205,21 @@ class Workload:
         return int(self.kv_pool.shape[0])
 
 
+def draw_queries(qs: Stream, T: int, Hi: int, Di: int, H: int, q_sigma: float = 1.0):
+    """Query-side inputs of T tokens from stream ``qs``: (q_idx e4m3 codes [T, Hi, Di], q_scale
+    [T, Hi], weights [T, Hi], q_mla bf16 bits [T, H, 576])."""
+    q_idx, q_scale = quantize_rows(qs.sub("q_idx").normal((T, Hi, Di)))
+    weights = qs.sub("weights").uniform((T, Hi))
+    q_mla = bf16_bits(qs.sub("q_mla").normal((T, H, D_QK), sigma=q_sigma))
+    return q_idx, q_scale, weights, q_mla
+
+
 def make_workload(name: str, B: int, ctx, queries, Hi: int, Di: int, H: int, topk: int,
-                  seed: int, q_sigma: float = 1.0, softmax_scale: float = 1.0 / math.sqrt(576.0)) -> Workload:
+                  seed: int, q_sigma: float = 1.0, softmax_scale: float = 1.0 / math.sqrt(576.0),
+                  query_stream: Stream | None = None) -> Workload:
     """Generic builder. ``queries[r]`` lists the absolute positions of request r's query tokens
-    (their token_kvlen is position + 1, so a query sees itself and everything before it)."""
+    (their token_kvlen is position + 1, so a query sees itself and everything before it).
+    The query-side values are drawn from ``query_stream`` (default: the workload's own stream)."""
     s = Stream(seed)
     ctx = np.asarray(ctx, dtype=np.int32)
     token_req = np.concatenate([np.full(len(q), r, np.int32) for r, q in enumerate(queries)])
@@ -216,18 +227,15 @@ def make_workload(name: str, B: int, ctx, queries, Hi: int, Di: int, H: int, top
     T = int(token_req.shape[0])
     bt, nblk = paged_block_tables(ctx, s.sub("pages"))
     ntok = int(ctx.sum())
-    # indexer
-    qi = s.sub("q_idx").normal((T, Hi, Di))
-    q_idx, q_scale = quantize_rows(qi)
-    weights = s.sub("weights").uniform((T, Hi))
+    q_idx, q_scale, weights, q_mla = draw_queries(query_stream or s, T, Hi, Di, H, q_sigma)
+    # indexer keys
     kk = s.sub("k").normal((ntok, Di))
     kc, ks = quantize_rows(kk)
     del kk
     k_cache = scatter_paged(kc, ctx, bt, nblk).reshape(nblk, PAGE, Di)
     k_scale = scatter_paged(ks, ctx, bt, nblk).reshape(nblk, PAGE)
     k_scale[k_scale == 0] = 1.0  # page tails: any positive scale
-    # sparse MLA
-    q_mla = bf16_bits(s.sub("q_mla").normal((T, H, D_QK), sigma=q_sigma))
+    # sparse MLA rows
     lat = s.sub("latent").normal((ntok, D_LATENT))
     rope = s.sub("rope").normal((ntok, D_ROPE))
     rows = pack_kv_rows(lat, rope)
@@ -265,10 +273,28 @@ def config4(chunk: int, seed: int = 4, total: int = 131072, chunk_len: int = 204
     """Long prefill from scratch: chunk `chunk` of total/chunk_len sequential chunks.
 
     The cache holds the whole sequence (same bytes for every chunk); the chunk's queries see
-    everything up to themselves."""
+    everything up to themselves. Each chunk's query values are its own draws."""
     ctx = np.array([total], np.int32)
     q = np.arange(chunk * chunk_len, (chunk + 1) * chunk_len)
-    return make_workload("long-prefill-chunk%d" % chunk, 1, ctx, [q], Hi, Di, H, topk, seed)
+    return make_workload("long-prefill-chunk%d" % chunk, 1, ctx, [q], Hi, Di, H, topk, seed,
+                         query_stream=Stream(seed).sub("chunk%d" % chunk))
+
+
+def config4_pass(seed: int = 4, total: int = 131072, chunk_len: int = 2048, Hi: int = 64, Di: int = 128,
+                 H: int = 64, topk: int = 2048, chunks=None) -> list:
+    """The chunks of one long-prefill pass (all total/chunk_len of them, or those listed), each
+    the Workload config4 would build for it; the cache arrays are built once and shared."""
+    n = total // chunk_len
+    chunks = list(range(n)) if chunks is None else list(chunks)
+    first = config4(chunks[0], seed, total, chunk_len, Hi, Di, H, topk)
+    out = [first]
+    for c in chunks[1:]:
+        qs = Stream(seed).sub("chunk%d" % c)
+        q_idx, q_scale, weights, q_mla = draw_queries(qs, chunk_len, Hi, Di, H)
+        kvlen = (np.arange(c * chunk_len, (c + 1) * chunk_len) + 1).astype(np.int32)
+        out.append(dataclasses.replace(first, name="long-prefill-chunk%d" % c, token_kvlen=kvlen, q_idx=q_idx,
+                                       q_scale=q_scale, weights=weights, q_mla=q_mla))
+    return out
 
 
 # ----------------------------------------------------------------------- HiSparse ------------

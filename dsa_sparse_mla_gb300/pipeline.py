@@ -4,7 +4,8 @@
 intermediate and output buffers and runs one step: hs_indexer_scores -> hs_topk ->
 hs_sparse_mla_fwd (logical indices through the paged block table); ``SharedSetHotPath`` runs the
 indexer and top-k for each request's final query token only and lets the request's other query
-tokens reuse that set in hs_sparse_mla_fwd (shared index sets). ``DeviceHiSparse`` does the
+tokens reuse that set in hs_sparse_mla_fwd (shared index sets); ``LongPrefillPass`` runs every
+chunk of a long prefill through the same three calls. ``DeviceHiSparse`` does the
 same for the mixed-residency decode (hs_hisparse_resolve -> hs_sparse_mla_fwd on physical rows),
 with the older rows in pinned host memory.
 
@@ -89,6 +90,63 @@ class HotPath:
         self.indexer(stream)
         self.topk(stream)
         self.mla(stream)
+
+
+class LongPrefillPass:
+    """One long-prefill pass: every chunk of one sequence through indexer -> top-k -> sparse MLA,
+    chunk after chunk. The sequence's K cache and KV pool and every chunk's query inputs stay
+    resident; the scores and top-k buffers are reused by each chunk, and the output holds the
+    whole sequence ([chunks, chunk_len, H, 512] bf16 and its LSE)."""
+
+    def __init__(self, chunks: list, device="cuda"):
+        w0 = chunks[0]
+        self.chunks = chunks
+        self.n = len(chunks)
+        self.T = w0.T
+        self.k_cache = _t(w0.k_cache, device)
+        self.k_scale = _t(w0.k_scale, device)
+        self.block_table = _t(w0.block_table, device)
+        self.token_req = _t(w0.token_req, device)
+        self.kv_pool = _t(w0.kv_pool, device)
+        self.q_idx = [_t(w.q_idx, device) for w in chunks]
+        self.q_scale = [_t(w.q_scale, device) for w in chunks]
+        self.weights = [_t(w.weights, device) for w in chunks]
+        self.q_mla = [_t(w.q_mla.view(np.int16), device).view(torch.bfloat16) for w in chunks]
+        self.token_kvlen = [_t(w.token_kvlen, device) for w in chunks]
+        ld = max(w.ld for w in chunks)
+        self.scores = torch.empty((w0.T, ld), dtype=torch.float32, device=device)
+        self.idx = torch.empty((w0.T, w0.topk), dtype=torch.int32, device=device)
+        self.out = torch.empty((self.n, w0.T, w0.H, 512), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((self.n, w0.T, w0.H), dtype=torch.float32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.workspace = torch.empty(hs_sparse_mla_workspace_size(w0.H), dtype=torch.uint8, device=device)
+
+    def step_inputs(self, c: int) -> list:
+        """The device tensors of chunk c that a serving loop would copy in for it."""
+        return [self.q_idx[c], self.q_scale[c], self.weights[c], self.q_mla[c], self.token_kvlen[c]]
+
+    def indexer(self, c: int, stream=None, q_idx=None, q_scale=None, weights=None, token_kvlen=None):
+        hs_indexer_scores(self.q_idx[c] if q_idx is None else q_idx, self.q_scale[c] if q_scale is None else q_scale,
+                          self.weights[c] if weights is None else weights, self.k_cache, self.k_scale,
+                          self.block_table, self.token_req,
+                          self.token_kvlen[c] if token_kvlen is None else token_kvlen, self.scores, self.err,
+                          num_requests=1, stream=stream)
+
+    def topk(self, c: int, stream=None, token_kvlen=None):
+        hs_topk(self.scores, self.token_kvlen[c] if token_kvlen is None else token_kvlen, self.chunks[c].topk,
+                self.idx, self.err, stream=stream)
+
+    def mla(self, c: int, stream=None, q_mla=None, out=None, lse=None):
+        hs_sparse_mla_fwd(self.q_mla[c] if q_mla is None else q_mla, self.kv_pool, self.idx,
+                          self.chunks[c].softmax_scale, self.out[c] if out is None else out, self.err,
+                          lse=self.lse[c] if lse is None else lse, block_table=self.block_table,
+                          token_req=self.token_req, workspace=self.workspace, stream=stream)
+
+    def step(self, stream=None):
+        for c in range(self.n):
+            self.indexer(c, stream)
+            self.topk(c, stream)
+            self.mla(c, stream)
 
 
 class SharedSetHotPath(HotPath):
