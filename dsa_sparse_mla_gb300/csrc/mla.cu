@@ -6,38 +6,39 @@
 // dims. Per query token t, head h, over the valid entries i of idx[t, :]:
 //   logit_i = scale * <q[t,h,:], [latent_i, rope_i]>,  out = softmax(logit) . latent,  lse = ln sum exp.
 //
-// One CTA per query token (416 threads):
-//   warps 0-7   gather 64 rows per tile (warp w owns rows 8w..8w+7; one 16-byte load per lane
-//               brings one 64-dim block of all 8 rows), dequantise latent = e4m3 * group scale to
-//               fp16 (exact e4m3 -> fp16 conversion, then code * scale rounded once to fp16 with
-//               the scale split into two fp16 parts; see dequant8_f16) and write it, with
-//               the bf16 RoPE part as stored, into a 128-byte-swizzled [dim block][row] tile
-//               (2 stages). Blocks are published in pairs as soon as they are written (a barrier
-//               per block), so QK starts on the first blocks while later ones are still being
-//               written; PV releases the stage pair by pair (one barrier per 128-dim M-tile),
-//               so the next tile's first blocks are written while PV still reads the last ones.
-//               Producers load the next tile into registers part by part as the current one is
-//               written, so global-memory latency is mostly off the MMA chain;
-//   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 64 rows,
-//               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile and an S
-//               buffer are ready;
-//   warps 9-12  first convert Q's latent dims to fp16 in shared memory (a head's row whose largest
-//               value fp16 cannot hold at full precision is scaled by a power of two), then run the online
-//               softmax: two threads share each head's row of S (one shuffle for the max); P goes
-//               as fp16 into the stage's RoPE block, which QK no longer needs, so P is double
-//               buffered with the stages. The last of the four warps to finish a tile (a counter
-//               in shared memory) issues O^T += V^T . P^T itself (M = 128 dims x4, N = 64 heads,
-//               K = 64 rows), so PV starts without a barrier hand-off to another warp, and QK of
-//               the next tiles, issued by warp 8, does not queue behind it. The same tile is the
-//               K-major B of QK and, read MN-major, the A of PV, so it is dequantised once. O^T
-//               lives in TMEM and is rescaled only when a head's running max grows by more than
-//               2^8 (lazy rescaling); the final pass divides by the row sum and writes bf16
-//               straight from TMEM (neighbouring lanes swap values so that each stores two
-//               adjacent dims of one head).
-// TMEM: columns 0-127 hold two S buffers (64-row layout), 128-383 hold O^T.
+// One CTA per query token (448 threads), rows in 32-row tiles through a ring of four stages:
+//   warps 0-7   gather the rows of each tile (warp w owns rows 4w..4w+3; lane l works on row
+//               4w + l / 8 and loads 16-byte pieces l % 8 of its 128-byte spans), dequantise
+//               latent = e4m3 * group scale to fp16 (exact e4m3 -> fp16 conversion, then
+//               code * scale rounded once, with the scale split into two fp16 parts; see
+//               dequant8_f16) and write it, with the bf16 RoPE part as stored, into a
+//               128-byte-swizzled [dim block][row] tile, once PV of the tile that used the stage
+//               four tiles before has completed. The whole tile is published with one proxy fence
+//               and one barrier arrival per warp (per-block-pair publication cost more in fences
+//               and waits than its overlap gained). The rows of tile i + 1 are loaded into the
+//               registers tile i leaves, part by part as tile i is written; rows are prefetched into
+//               L2 three tiles ahead;
+//   warp 8      allocates TMEM, loads Q by TMA and issues S = Q . K^T (M = 64 heads, N = 32 rows,
+//               K = 512 fp16 latent + 64 bf16 RoPE; A = Q, B = tile) as soon as a tile is written
+//               and an S buffer is free, so QK of later tiles runs while the softmax works on
+//               earlier ones;
+//   warp 9      issues O^T += V^T . P^T (M = 128 dims x4, N = 64 heads, K = 32 rows) for each tile
+//               once its P is written; its completion releases the stage. All PV
+//               MMAs come from this one thread, so they accumulate in order without waiting on one
+//               another; the same tile is the K-major B of QK and, read MN-major, the A of PV, so it
+//               is dequantised once;
+//   warps 10-13 first convert Q's latent dims to fp16 in shared memory (a head's row whose largest
+//               value fp16 cannot hold at full precision is scaled by a power of two), then run the
+//               online softmax: two threads share each head's row of S (one shuffle for the max); P
+//               goes as fp16 into the stage's RoPE block, which QK no longer needs (K-major, 64-byte
+//               swizzle). O^T lives in TMEM and is rescaled only when a head's running max grows by
+//               more than 2^8 (lazy rescaling), after the previous tile's PV has completed; the final
+//               pass divides by the row sum and writes bf16 straight from TMEM (neighbouring lanes
+//               swap values so that each stores two adjacent dims of one head).
+// TMEM: columns 0-127 hold four S buffers (64-row layout, 32 columns each), 128-383 hold O^T.
 //
 // Work split (launch_mla): one CTA per query when the queries fill their waves; otherwise, given a
-// workspace, one persistent CTA per SM takes an equal share of all (query, 64-row tile) units, a
+// workspace, one persistent CTA per SM takes an equal share of all (query, 32-row tile) units, a
 // query split between CTAs leaves a normalised partial and its LSE per CTA, and mla_merge_kernel
 // combines them (split-KV decode: DCP's log-sum-exp merge on one GPU).
 #include "common.cuh"
@@ -45,37 +46,40 @@
 namespace hs {
 namespace mla {
 
-constexpr int kRows = 64;
+constexpr int kRows = 32;                  // rows per tile
+constexpr int kStages = 4;
 constexpr int kProdWarps = 8;
 constexpr int kMmaWarp = kProdWarps;       // QK issuer; also allocates TMEM
-constexpr int kSmThreads = 128;            // softmax / epilogue warps; the last one done with a tile issues its PV
-constexpr int kThreads = 32 * (kProdWarps + 1 + 4);
+constexpr int kPvWarp = kProdWarps + 1;    // PV issuer
+constexpr int kSmThreads = 128;
+constexpr int kThreads = 32 * (kProdWarps + 2 + 4);  // + QK warp, PV warp, 4 softmax warps
 constexpr uint32_t kColS = 0;
 constexpr uint32_t kColO = 128;
-constexpr int kBlk = 8192;                 // one [64 rows][128 B] swizzled block
-constexpr int kQBytes = 9 * kBlk;          // 64 heads x 576 bf16
-constexpr int kStageBytes = 9 * kBlk;      // 64 rows x (512 latent + 64 rope) bf16
+constexpr int kQBlk = 8192;                // one [64 heads][128 B] swizzled block of Q
+constexpr int kBlk = kRows * 128;          // one [32 rows][128 B] swizzled block of a stage
+constexpr int kQBytes = 9 * kQBlk;         // 64 heads x 576 bf16
+constexpr int kStageBytes = 9 * kBlk;      // 32 rows x (512 latent + 64 rope) fp16/bf16
 constexpr int kBlocks = 9;                 // 8 latent dim blocks + the RoPE block (later P)
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kQBytes;
-constexpr int kOffValid = kOffStage + 2 * kStageBytes;  // uint8 [2][64]
-constexpr int kOffAlpha = kOffValid + 128;          // float [64]
-constexpr int kOffInvL = kOffAlpha + 256;           // float [64]
-constexpr int kOffQe = kOffInvL + 256;              // int [64]: per-head exponent e of the current query
-constexpr int kEmpty = 5;                 // per stage: 4 latent block pairs (one PV M-tile each) + RoPE/P
-constexpr int kNumBars = 2 * kBlocks + 2 * kEmpty + 10;
+constexpr int kOffValid = kOffStage + kStages * kStageBytes;  // uint8 [kStages][32]
+constexpr int kOffAlpha = kOffValid + kStages * kRows;        // float [64]
+constexpr int kOffInvL = kOffAlpha + 256;                     // float [64]
+constexpr int kOffQe = kOffInvL + 256;                        // int [64]: per-head exponent of the current query
+constexpr int kNumBars = 6 * kStages + 5;
 constexpr int kOffBar = kOffQe + 256;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem base, abort, P counter
+constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort
 constexpr int kSmem = kOffMisc + 16 + 1024;
-constexpr float kRescaleThreshold = 8.0f;           // log2 units
+constexpr float kRescaleThreshold = 8.0f;         // log2 units
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kScaleMax = 65504.f / 448.f;     // |code * scale| stays finite in fp16
-constexpr float kScaleMin = 6.103515625e-05f;    // 2^-14: scales stay fp16 normals
+constexpr float kScaleMax = 65504.f / 448.f;      // |code * scale| stays finite in fp16
+constexpr float kScaleMin = 6.103515625e-05f;     // 2^-14: scales stay fp16 normals
+static_assert(kSmem <= 232448, "shared memory");
 
 struct Params {
   int32_t T, H, k;
-  const __nv_bfloat16* q;  // [T][H][576], also loaded by TMA; read directly for the per-head maxima
+  const __nv_bfloat16* q;  // [T][H][576], also loaded by TMA; read directly to rescale a head's row
   const uint8_t* kv;
   int64_t R;
   const int32_t* idx;
@@ -89,7 +93,7 @@ struct Params {
   __nv_bfloat16* out;
   float* lse;
   int32_t* err;
-  // Work split. Units are (query, 64-row tile) pairs, U = T * tiles per query in total. A CTA
+  // Work split. Units are (query, 32-row tile) pairs, U = T * tiles per query in total. A CTA
   // takes the units [c U / C, (c + 1) U / C) (persistent launch, C CTAs) or exactly the units of
   // query c (one CTA per query). A query whose units span several CTAs leaves, from each, its
   // softmax-normalised partial output (bf16) and log-sum-exp in a workspace slot (2c for the
@@ -123,13 +127,26 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t w0, uint32_t w1, uint32_t
   return r;
 }
 
-// One softmax warp's arrival on the tile counter (four per tile); true for the last of the four.
-// Each warp's P stores (already fenced for the async proxy) and TMEM accesses precede its release,
-// and the last arriver acquires them all before it issues the tile's PV.
-__device__ __forceinline__ bool arrive_last(uint32_t* ctr) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(old) : "r"(smem_u32(ctr)) : "memory");
-  return (old & 3u) == 3u;
+// The rows of one tile a producer lane holds: four 16-byte latent pieces (bytes 128 j + 16 (l % 8)
+// of its row, j = 0..3), its 16-byte RoPE piece and the row's four group scales.
+struct TileRegs {
+  uint4 lat[4];
+  uint4 rope;
+  uint4 scl;
+};
+
+// Segment walk shared by every role: the CTA's units [u0, u1) as queries q with tiles [ta, tb).
+struct Seg {
+  int64_t q;
+  int ta, tb;
+};
+__device__ __forceinline__ Seg next_seg(int64_t& u, int64_t u1, int ntq) {
+  Seg g;
+  g.q = u / ntq;
+  g.ta = (int)(u - g.q * ntq);
+  g.tb = (int)((u1 - g.q * ntq) < ntq ? (u1 - g.q * ntq) : ntq);
+  u = g.q * ntq + g.tb;
+  return g;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -143,19 +160,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sInvL = (float*)(smem + kOffInvL);
   int32_t* sQe = (int32_t*)(smem + kOffQe);
   uint64_t* bars = (uint64_t*)(smem + kOffBar);
-  uint64_t* full = bars + 0;                 // [2][9] producers wrote dim block b -> QK
-  uint64_t* empty = bars + 2 * kBlocks;      // [2][5] PV done with block pair m (m = 4: RoPE/P) -> producers
-  uint64_t* s_full = empty + 2 * kEmpty;     // [2] QK done -> softmax
-  uint64_t* s_free = s_full + 2;             // [2] softmax read S -> MMA
-  uint64_t* pv_done = s_full + 4;            // PV done -> softmax
-  uint64_t* q_full = s_full + 5;
-  uint64_t* mma_done = s_full + 6;           // QK issuer's MMAs drained
-  uint64_t* pv_drain = s_full + 7;           // PV MMAs of every softmax warp drained
-  uint64_t* q_ready = s_full + 8;            // Q converted to fp16 (latent dims) -> QK issuer
-  uint64_t* q_free = s_full + 9;             // QK MMAs of a query finished reading Q -> QK issuer
+  uint64_t* full = bars + 0;                       // [4] producers wrote the stage's tile -> QK, softmax
+  uint64_t* empty = full + kStages;                // [4] PV of the stage's tile complete -> producers, softmax
+  uint64_t* s_full = empty + kStages;              // [4] QK done -> softmax
+  uint64_t* s_free = s_full + kStages;             // [4] softmax read S -> QK
+  uint64_t* p_ready = s_free + kStages;            // [4] softmax wrote P (and rescaled O^T) -> PV
+  uint64_t* q_full = p_ready + kStages;
+  uint64_t* mma_done = q_full + 1;                 // QK issuer's MMAs drained
+  uint64_t* pv_drain = q_full + 2;                 // PV issuer's MMAs drained
+  uint64_t* q_ready = q_full + 3;                  // Q converted to fp16 (latent dims) -> QK issuer
+  uint64_t* q_free = q_full + 4;                   // QK MMAs of a query finished reading Q -> QK issuer
   uint32_t* misc = (uint32_t*)(smem + kOffMisc);
   volatile uint32_t* abort_flag = misc + 1;
-  uint32_t* p_count = misc + 2;              // softmax warps' tile completions (4 per tile)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k = p.k;
@@ -173,21 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntot = (int)(u1 - u0);  // tiles of this CTA
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * kBlocks; ++i) mbar_init(&full[i], kProdWarps);
-    for (int i = 0; i < 2 * kEmpty; ++i) mbar_init(&empty[i], 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], kProdWarps);
+      mbar_init(&empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
+      mbar_init(&p_ready[i], 4);
     }
-    mbar_init(pv_done, 1);
     mbar_init(q_full, 1);
     mbar_init(mma_done, 1);
-    mbar_init(pv_drain, kSmThreads / 32);
+    mbar_init(pv_drain, 1);
     mbar_init(q_ready, 4);
     mbar_init(q_free, 1);
     mbar_fence_init();
     misc[1] = 0;
-    misc[2] = 0;
   }
   if (warp == kMmaWarp) tmem_alloc(&misc[0], 512);
   __syncthreads();
@@ -196,56 +211,60 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kProdWarps) {
     // ================================================================ gather + dequantise ======
-    // Warp w owns rows 8w .. 8w+7 of every tile. Lane l works on row 8w + (l >> 2): for dim block
-    // b (64 latent dims) it loads bytes [64b + 16(l & 3), +16) of that row, so one instruction
-    // brings block b of all 8 rows. The RoPE part (128 bytes a row) takes two instructions
-    // (lane l: row 8w + 4h + (l >> 3), bytes 16(l & 7)..), the group scales one (lanes 0-7).
-    // Software pipeline per warp:
-    //   tile i+4: index entries (lanes 0-7)     tile i+3: block-table entries
-    //   tile i+2: rows prefetched into L2 by the TMA engine (one 656-byte bulk prefetch per row)
+    // Warp w owns rows 4w .. 4w+3 of every tile; lane l works on row 4w + rl, rl = l / 8, and
+    // loads bytes 128 j + 16 c8 (c8 = l % 8, j = 0..3) of its latent codes: 16 codes of dim block
+    // 2j + c8 / 4, i.e. 16-byte chunks 2 (c8 % 4) and 2 (c8 % 4) + 1 of that block's fp16 row
+    // (group scale j). Its RoPE piece is bytes 16 c8 of the row's RoPE part (chunk c8 of the RoPE
+    // block); each lane also loads its row's four scales (the eight lanes of a row read the same
+    // 16 bytes, one transaction). Lanes 0-3 carry the index pipeline of rows 4w .. 4w+3:
+    //   tile i+5: index entries (and visible lengths)   tile i+4: block-table entries
+    //   tile i+1 .. i+3: rows prefetched into L2 by the TMA engine (one 656-byte bulk prefetch
+    //             per row, three tiles ahead)
     //   tile i+1: row data loaded into registers, each part as soon as tile i's part in those
-    //             registers has been written (so most of the loads are in flight while the
-    //             rest of the stage is still being released)
-    //   tile i  : dequantised into its stage, block by block, once the stage is free.
+    //             registers has been written
+    //   tile i  : dequantised into stage i % 4 once PV of tile i-4 has completed.
+    // Every loaded value is first used one step after its load, so no step waits on a load
+    // issued in the same step.
     // Loads are volatile so they are issued here and not next to their first use.
-    const int sub = lane & 3;          // 16-byte piece of a 64-byte latent block
-    const int rlat = lane >> 2;        // row (within the warp's 8) of the latent pieces
-    const int rrope = lane >> 3;       // row (within a 4-row half) of the RoPE pieces
-    // lane rr < 8: index entry of row 8 * warp + rr of the CTA's next lookahead tile (tiles are
-    // visited in order: la_q / la_t are that tile's query and tile), and (with a block table) the
-    // request of its query
+    const int rl = lane >> 3, c8 = lane & 7;
+    const int row = warp * 4 + rl;   // this lane's row within a tile
     int64_t la_q = u0 / ntq;
     int la_t = (int)(u0 - la_q * ntq), la_n = 0;
-    auto ld_idx = [&](int32_t& req) -> int32_t {
+    // lanes 0-3: index entry of row 4 * warp + lane of the CTA's next lookahead tile (tiles are
+    // visited in order) and, with a block table, the request of its query
+    auto ld_idx = [&](int32_t& req, int32_t& lim) -> int32_t {
       req = 0;
+      lim = 0x7FFFFFFF;
       const bool live = la_n < ntot;
       const int64_t q = la_q;
-      const int e = la_t * kRows + warp * 8 + lane;
+      const int e = la_t * kRows + warp * 4 + lane;
       if (++la_t == ntq) {
         la_t = 0;
         ++la_q;
       }
       ++la_n;
-      if (lane >= 8 || !live || e >= k) return -1;
-      int64_t row = q;
+      if (lane >= 4 || !live || e >= k) return -1;
+      int64_t r = q;
       if (p.idx_row) {
-        row = ldg_nc_s32(p.idx_row + q);
-        if (row < 0 || row >= p.idx_rows) {
+        r = ldg_nc_s32(p.idx_row + q);
+        if (r < 0 || r >= p.idx_rows) {
           flag_error(p.err, HS_FLAG_BAD_INDEX);
           return -1;
         }
       }
       if (p.bt) req = ldg_nc_s32(p.token_req + q);
-      const int32_t j = ldg_nc_s32(p.idx + row * k + e);
-      return p.kvlen && j >= ldg_nc_s32(p.kvlen + q) ? -1 : j;
+      const int32_t j = ldg_nc_s32(p.idx + r * k + e);
+      if (p.kvlen) lim = ldg_nc_s32(p.kvlen + q);  // applied one step later, in ld_blk
+      return j;
     };
-    auto ld_blk = [&](int32_t j, int32_t req) -> int32_t {  // lanes 0-7: block-table entry of entry j (j if none)
-      if (lane >= 8 || j < 0 || !p.bt) return j;
+    auto ld_blk = [&](int32_t& j, int32_t req, int32_t lim) -> int32_t {  // lanes 0-3: block-table entry of entry j (j if none)
+      if (j >= lim) j = -1;  // beyond the query's visible length
+      if (lane >= 4 || j < 0 || !p.bt) return j;
       const int32_t page = j >> 6;
       return page < p.bt_stride ? ldg_nc_s32(p.bt + (int64_t)req * p.bt_stride + page) : -1;
     };
-    auto phys_row = [&](int32_t j, int32_t b) -> int64_t {  // lanes 0-7: physical row, -1 if none
-      if (lane >= 8 || j < 0) return -1;
+    auto phys_row = [&](int32_t j, int32_t b) -> int64_t {  // lanes 0-3: physical row, -1 if none
+      if (lane >= 4 || j < 0) return -1;
       const int64_t r = p.bt ? (b >= 0 ? (int64_t)b * 64 + (j & 63) : -1) : (int64_t)j;
       if (r < 0 || r >= p.R) {
         flag_error(p.err, HS_FLAG_BAD_INDEX);
@@ -253,135 +272,103 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return r;
     };
-    uint4 lat[8];              // next tile: latent block b of row rlat (16 codes)
-    uint4 rope[2];             // next tile: RoPE half h, row 4h + rrope (8 bf16)
-    float4 scl = make_float4(0.f, 0.f, 0.f, 0.f);  // lanes 0-7: group scales of row lane
-    int64_t my_row = -1;       // lanes 0-7: physical row of the tile whose data is loaded
-    auto ld_rows = [&](int64_t rows_lane) {
-      const int64_t r0 = __shfl_sync(0xffffffffu, rows_lane, rlat);
-      const int64_t r1 = __shfl_sync(0xffffffffu, rows_lane, rrope);
-      const int64_t r2 = __shfl_sync(0xffffffffu, rows_lane, 4 + rrope);
-      const uint8_t* src = p.kv + (r0 >= 0 ? r0 : 0) * HS_KV_ROW_BYTES + 16 * sub;
-#pragma unroll
-      for (int b = 0; b < 8; ++b) lat[b] = r0 >= 0 ? ldg_nc_v4(src + 64 * b) : make_uint4(0, 0, 0, 0);
-      rope[0] = r1 >= 0 ? ldg_nc_v4(p.kv + r1 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
-                        : make_uint4(0, 0, 0, 0);
-      rope[1] = r2 >= 0 ? ldg_nc_v4(p.kv + r2 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
-                        : make_uint4(0, 0, 0, 0);
-      if (lane < 8 && rows_lane >= 0) {
-        const uint4 v = ldg_nc_v4(p.kv + rows_lane * HS_KV_ROW_BYTES + HS_D_LATENT);
-        scl = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
-      } else {
-        scl = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+    auto prefetch_rows = [&](int64_t r) {
+      if (r >= 0) bulk_prefetch_l2(p.kv + r * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
     };
-    // dequantises the loaded rows into stage i % 2 block by block: each block pair is written as
-    // soon as PV of the tile that used the stage before has released it, and published at once;
-    // false on abort
-    auto wait_empty = [&](int s, int m, int i) -> bool {
+    // this lane's row of a tile from the lanes 0-3 row values
+    auto row_of = [&](int64_t rows_lane) -> int64_t { return __shfl_sync(0xffffffffu, rows_lane, rl); };
+    auto ld_lat = [&](int64_t r, int j) -> uint4 {
+      return r >= 0 ? ldg_nc_v4(p.kv + r * HS_KV_ROW_BYTES + 128 * j + 16 * c8) : make_uint4(0, 0, 0, 0);
+    };
+    auto ld_rope = [&](int64_t r) -> uint4 {
+      return r >= 0 ? ldg_nc_v4(p.kv + r * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * c8) : make_uint4(0, 0, 0, 0);
+    };
+    auto ld_scl = [&](int64_t r) -> uint4 {
+      return r >= 0 ? ldg_nc_v4(p.kv + r * HS_KV_ROW_BYTES + HS_D_LATENT) : make_uint4(0, 0, 0, 0);
+    };
+    auto ld_tile = [&](TileRegs& t, int64_t rows_lane) {
+      const int64_t r = row_of(rows_lane);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t.lat[j] = ld_lat(r, j);
+      t.rope = ld_rope(r);
+      t.scl = ld_scl(r);
+    };
+    auto wait_empty = [&](int s, int i) -> bool {
       int go = 1;
-      if (lane == 0) go = !*abort_flag && mbar_wait(&empty[s * kEmpty + m], ((uint32_t)(i >> 1) & 1u) ^ 1u, p.err);
+      if (lane == 0) go = !*abort_flag && mbar_wait(&empty[s], ((uint32_t)(i >> 2) & 1u) ^ 1u, p.err);
       go = __shfl_sync(0xffffffffu, go, 0);
       if (!go && lane == 0) *abort_flag = 1;
       return go != 0;
     };
-    auto publish = [&](int i, int64_t next_row) -> bool {
-      const int s = i & 1;
-      // tile i+1's rows are loaded into the registers tile i's rows leave, as soon as each part
-      // has been written: the loads are in flight while the rest of the stage is released
-      const int64_t n0 = __shfl_sync(0xffffffffu, next_row, rlat);
-      const uint8_t* nsrc = p.kv + (n0 >= 0 ? n0 : 0) * HS_KV_ROW_BYTES + 16 * sub;
-      if (!wait_empty(s, 0, i)) return false;
+    // Writes tile i (in t, rows cur_rows on lanes 0-3) into stage i % 4 and loads tile i + 1
+    // (rows next_rows) into t part by part as each part is written; false on abort.
+    auto publish = [&](int i, TileRegs& t, int64_t cur_rows, int64_t next_rows) -> bool {
+      const int s = i & 3;
+      const int64_t nr = row_of(next_rows);
+      if (!wait_empty(s, i)) return false;  // PV of tile i - 4 complete
       uint8_t* st = sStage + s * kStageBytes;
-      uint64_t* fb = full + s * kBlocks;
-      if (lane < 8) sValid[s * kRows + warp * 8 + lane] = my_row >= 0 ? 1 : 0;
-      const int row = warp * 8 + rlat;
+      if (lane < 4) sValid[s * kRows + warp * 4 + lane] = cur_rows >= 0 ? 1 : 0;
       bool range_ok = true;
+      const float scales[4] = {__uint_as_float(t.scl.x), __uint_as_float(t.scl.y), __uint_as_float(t.scl.z),
+                               __uint_as_float(t.scl.w)};
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        if (g > 0 && !wait_empty(s, g, i)) return false;
-        const float sg = g == 0 ? scl.x : g == 1 ? scl.y : g == 2 ? scl.z : scl.w;
-        const float scale = __shfl_sync(0xffffffffu, sg, rlat);
+      for (int j = 0; j < 4; ++j) {
+        const float scale = scales[j];
         range_ok &= scale == 0.f || (fabsf(scale) >= kScaleMin && fabsf(scale) <= kScaleMax);
         const __half shi = __float2half_rn(scale);
         const __half2 h2 = __half2half2(shi);
         const __half2 l2 = __float2half2_rn(scale - __half2float(shi));  // scale - hi is exact in fp32
         const uint32_t h2u = *reinterpret_cast<const uint32_t*>(&h2);
         const uint32_t l2u = *reinterpret_cast<const uint32_t*>(&l2);
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb) {
-          const int b = 2 * g + bb;
-          const uint4 v = lat[b];
-          const uint4 lo = dequant8_f16(v.x, v.y, h2u, l2u);
-          const uint4 hi = dequant8_f16(v.z, v.w, h2u, l2u);
-          uint8_t* blk = st + b * kBlk;
-          *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * sub)) = lo;
-          *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * sub + 16)) = hi;
-        }
-        // publish the pair (one proxy fence per pair: each fence + arrive costs ~50 cycles)
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&fb[2 * g]);
-          mbar_arrive(&fb[2 * g + 1]);
-        }
-#pragma unroll
-        for (int bb = 0; bb < 2; ++bb)
-          lat[2 * g + bb] = n0 >= 0 ? ldg_nc_v4(nsrc + 64 * (2 * g + bb)) : make_uint4(0, 0, 0, 0);
+        const uint4 v = t.lat[j];
+        const uint4 lo = dequant8_f16(v.x, v.y, h2u, l2u);
+        const uint4 hi = dequant8_f16(v.z, v.w, h2u, l2u);
+        uint8_t* blk = st + (2 * j + (c8 >> 2)) * kBlk;
+        *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * (c8 & 3))) = lo;
+        *reinterpret_cast<uint4*>(blk + sw128_offset(row, 32 * (c8 & 3) + 16)) = hi;
+        t.lat[j] = ld_lat(nr, j);
       }
-      if (lane < 8 && next_row >= 0) {
-        const uint4 v = ldg_nc_v4(p.kv + next_row * HS_KV_ROW_BYTES + HS_D_LATENT);
-        scl = make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
-      } else {
-        scl = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      // RoPE block (bf16 as stored); it held P of the tile before, released last
-      if (!wait_empty(s, 4, i)) return false;
-      *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(warp * 8 + rrope, 16 * (lane & 7))) = rope[0];
-      *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(warp * 8 + 4 + rrope, 16 * (lane & 7))) = rope[1];
+      // RoPE block (bf16 as stored); it held P of tile i - 4
+      *reinterpret_cast<uint4*>(st + 8 * kBlk + sw128_offset(row, 16 * c8)) = t.rope;
       if (!range_ok) flag_error(p.err, HS_FLAG_RANGE);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&fb[8]);
-      {
-        const int64_t r1 = __shfl_sync(0xffffffffu, next_row, rrope);
-        const int64_t r2 = __shfl_sync(0xffffffffu, next_row, 4 + rrope);
-        rope[0] = r1 >= 0 ? ldg_nc_v4(p.kv + r1 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
-                          : make_uint4(0, 0, 0, 0);
-        rope[1] = r2 >= 0 ? ldg_nc_v4(p.kv + r2 * HS_KV_ROW_BYTES + HS_D_LATENT + 16 + 16 * (lane & 7))
-                          : make_uint4(0, 0, 0, 0);
-      }
+      if (lane == 0) mbar_arrive(&full[s]);
+      t.rope = ld_rope(nr);
+      t.scl = ld_scl(nr);
       return true;
     };
-    // prologue: tile 0 in registers, tile 1 prefetched into L2, tile 2 block entries and tile 3
-    // index entries in flight
-    {
-      int32_t r0;
-      const int32_t j0 = ld_idx(r0);
-      my_row = phys_row(j0, ld_blk(j0, r0));
-    }
-    ld_rows(my_row);
-    int64_t row_next;  // lanes 0-7: physical row of tile i+1 (already prefetched)
-    {
-      int32_t r1;
-      const int32_t j1 = ld_idx(r1);
-      row_next = phys_row(j1, ld_blk(j1, r1));
-      if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
-    }
-    int32_t rA, rB;
-    int32_t jA = ld_idx(rA);
-    int32_t bA = ld_blk(jA, rA);  // block-table entries travel with their index entries
-    int32_t jB = ld_idx(rB);
+    // prologue: index entries of tiles 0-5, block-table entries of tiles 0-4; tile 0 into the
+    // registers, tiles 1-3 prefetched into L2
+    int32_t jt[6], rq[6], lm[6];
+#pragma unroll
+    for (int x = 0; x < 6; ++x) jt[x] = ld_idx(rq[x], lm[x]);
+    int32_t bt[5];
+#pragma unroll
+    for (int x = 0; x < 5; ++x) bt[x] = ld_blk(jt[x], rq[x], lm[x]);
+    int64_t rowc = phys_row(jt[0], bt[0]);  // lanes 0-3: rows of the tile in the registers
+    TileRegs A;
+    ld_tile(A, rowc);
+    int64_t r1 = phys_row(jt[1], bt[1]);
+    int64_t r2 = phys_row(jt[2], bt[2]);
+    int64_t r3 = phys_row(jt[3], bt[3]);
+    prefetch_rows(r1);
+    prefetch_rows(r2);
+    prefetch_rows(r3);
+    int32_t j4 = jt[4], b4 = bt[4];
+    int32_t j5 = jt[5], q5 = rq[5], l5 = lm[5];
     for (int i = 0; i < ntot; ++i) {
-      // publishes tile i and leaves tile i+1 in registers (from L2); then tile i+2 into L2,
-      // tile i+3 block entries, tile i+4 index entries
-      if (!publish(i, row_next)) break;
-      my_row = row_next;
-      row_next = phys_row(jA, bA);
-      if (row_next >= 0) bulk_prefetch_l2(p.kv + row_next * HS_KV_ROW_BYTES, HS_KV_ROW_BYTES);
-      jA = jB;
-      bA = ld_blk(jB, rB);
-      jB = ld_idx(rB);  // tile i + 4
+      const int64_t n1 = r1;
+      if (!publish(i, A, rowc, n1)) break;
+      rowc = n1;
+      const int64_t r4 = phys_row(j4, b4);
+      prefetch_rows(r4);
+      r1 = r2;
+      r2 = r3;
+      r3 = r4;
+      b4 = ld_blk(j5, q5, l5);
+      j4 = j5;
+      j5 = ld_idx(q5, l5);
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ QK issuer =================
@@ -394,9 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int seg = 0, i = 0;  // segment and global tile counters
 #pragma unroll 1
       for (int64_t u = u0; u < u1 && ok; ++seg) {
-        const int64_t q = u / ntq;
-        const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
-        u = q * ntq + tb;
+        const Seg g = next_seg(u, u1, ntq);
         if (seg > 0) {  // the previous query's QK MMAs must have read Q before it is replaced
           mma_commit(q_free);
           if (!mbar_wait(q_free, (uint32_t)(seg - 1) & 1u, p.err)) {
@@ -406,73 +391,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(q_full, kQBytes);
 #pragma unroll 1
-        for (int db = 0; db < 9; ++db) tma_load_2d(sQ + db * kBlk, &map_q, q_full, db * 64, (int32_t)(q * p.H));
+        for (int db = 0; db < 9; ++db)
+          tma_load_2d(sQ + db * kQBlk, &map_q, q_full, db * 64, (int32_t)(g.q * p.H));
         if (!mbar_wait(q_ready, (uint32_t)seg & 1u, p.err)) {
           ok = false;
           break;
         }
 #pragma unroll 1
-      for (int jt = ta; jt < tb; ++jt, ++i) {
-        const int s = i & 1;
-        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
-        if (*abort_flag || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
-          ok = false;
-          break;
-        }
-        const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
-        const uint32_t d = tmem + kColS + 64 * s;
-#pragma unroll
-        for (int db = 0; db < kBlocks; ++db) {
-          // dim block db of this tile written by all producer warps
-          if (!mbar_wait(&full[s * kBlocks + db], ph, p.err)) {
+        for (int jt = g.ta; jt < g.tb; ++jt, ++i) {
+          const int s = i & 3;
+          const uint32_t ph = (uint32_t)(i >> 2) & 1u;
+          if (*abort_flag || !mbar_wait(&s_free[s], ph ^ 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
+          const uint32_t d = tmem + kColS + kRows * s;
+          if (!mbar_wait(&full[s], ph, p.err)) {  // the whole tile written by all producer warps
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = smem_desc(q_addr + db * kBlk + kk * 32, 16, 1024, 2);
-            const uint64_t b = smem_desc(sa + db * kBlk + kk * 32, 16, 1024, 2);
-            mma_bf16_ss(d, a, b, db < 8 ? idesc_qk : idesc_qk_rope, (db | kk) != 0 ? 1u : 0u);
+          for (int db = 0; db < kBlocks; ++db) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = smem_desc(q_addr + db * kQBlk + kk * 32, 16, 1024, 2);
+              const uint64_t b = smem_desc(sa + db * kBlk + kk * 32, 16, 1024, 2);
+              mma_bf16_ss(d, a, b, db < 8 ? idesc_qk : idesc_qk_rope, (db | kk) != 0 ? 1u : 0u);
+            }
           }
+          if (!ok) break;
+          mma_commit(&s_full[s]);
         }
-        if (!ok) break;
-        mma_commit(&s_full[s]);
-      }
       }
       if (!ok) *abort_flag = 1;
       mma_commit(mma_done);
       mbar_wait(mma_done, 0, p.err);
       if (seg > 0) mbar_wait(q_full, (uint32_t)(seg - 1) & 1u, p.err);  // the last Q copy has landed
     }
+  } else if (warp == kPvWarp) {
+    // ================================================================ PV issuer =================
+    // O^T += V^T . P^T for each tile once the softmax warps have written its P: the stage read
+    // MN-major as A (M = 128 dims x4 M-tiles, K = 32 rows in two steps), P^T from the stage's
+    // RoPE block as B (K-major, 64-byte swizzle, N = 64 heads). The first tile of a query starts
+    // O^T afresh. One commit per tile marks its PV complete, which releases the whole stage
+    // (the producers refill it, and a softmax warp about to rescale O^T waits for it).
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
+      const uint32_t st_addr = smem_u32(sStage);
+      bool ok = true;
+      int i = 0;
+#pragma unroll 1
+      for (int64_t u = u0; u < u1 && ok;) {
+        const Seg g = next_seg(u, u1, ntq);
+#pragma unroll 1
+        for (int jt = g.ta; jt < g.tb; ++jt, ++i) {
+          const int s = i & 3;
+          if (*abort_flag || !mbar_wait(&p_ready[s], (uint32_t)(i >> 2) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
+          const uint32_t p_addr = sa + 8 * kBlk;  // P of this tile in the stage's RoPE block
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+            for (int kk = 0; kk < kRows / 16; ++kk) {
+              const uint64_t a = smem_desc(sa + (uint32_t)(2 * mt * kBlk + kk * 2048), kBlk, 1024, 2);
+              const uint64_t b = smem_desc(p_addr + kk * 32, 16, 512, 4);
+              mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (jt > g.ta || kk > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&empty[s]);  // the tile's PV is complete: the stage (and P in it) may be refilled
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(pv_drain);
+      mbar_wait(pv_drain, 0, p.err);
+    }
   } else {
     // ================================================================ softmax / epilogue ========
-    // Head h = 16 * quad + (lane % 16); lanes l and l + 16 share it, each owning 32 of the
-    // tile's 64 columns (TMEM 16x32bx2 load), so the running max is agreed by one shuffle.
+    // Head h = 16 * quad + (lane % 16); lanes l and l + 16 share it, each owning 16 of the tile's
+    // 32 columns (TMEM 16x32bx2 load), so the running max is agreed by one shuffle.
     const int quad = warp & 3;
     const int hl = lane & 15, half = lane >> 4;
     const int h = quad * 16 + hl;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    constexpr uint32_t idesc_pv = idesc_f16(128, 64, 1, 0);
-    const uint32_t st_addr = smem_u32(sStage);
+    const int sm_tid = tid - (kThreads - kSmThreads);
     bool ok = true;
     int seg = 0, i = 0;  // segment and global tile counters
+    // true once PV of global tile j has completed (its commit releases the stage)
+    auto wait_pv = [&](int j) -> bool {
+      return warp_wait(&empty[j & 3], (uint32_t)(j >> 2) & 1u, p.err, lane);
+    };
 #pragma unroll 1
     for (int64_t u = u0; u < u1 && ok; ++seg) {
-      const int64_t q = u / ntq;
-      const int tb = (int)((u1 - q * ntq) < ntq ? (u1 - q * ntq) : ntq), ta = (int)(u - q * ntq);
-      u = q * ntq + tb;
-      // Q's latent dims (blocks 0-7) bf16 -> fp16 in place. Chunk c = sm_tid + 128 j (16 bytes) is dim
-      // block j / 4 of head row (sm_tid / 8) + 16 (j % 4), so the 8 lanes sm_tid & ~7 .. + 7 hold all
-      // of a row's chunks and agree on its largest |q| with three shuffles. A row whose largest
-      // value lies outside [2^-6, 2^15) (rare: fp16 would overflow, or lose precision to its
+      const Seg g = next_seg(u, u1, ntq);
+      const int64_t q = g.q;
+      const int ta = g.ta, tb = g.tb;
+      // Q's latent dims (blocks 0-7) bf16 -> fp16 in place. Chunk c = sm_tid + 128 j (16 bytes) is
+      // dim block j / 4 of head row (sm_tid / 8) + 16 (j % 4), so the 8 lanes sm_tid & ~7 .. + 7
+      // hold all of a row's chunks and agree on its largest |q| with three shuffles. A row whose
+      // largest value lies outside [2^-6, 2^15) (rare: fp16 would overflow, or lose precision to its
       // subnormal range) is then rewritten from global memory scaled by an exact power of two 2^e
       // that puts its largest value in [2^14, 2^15), RoPE block included (bf16, exact); the softmax
       // multiplies that head's logits by 2^-e. Other rows keep e = 0.
       float sc_log2;  // softmax scale * log2(e) * 2^-e of this thread's head
       {
         const bool qok = warp_wait(q_full, (uint32_t)seg & 1u, p.err, lane);
-        const int sm_tid = tid - (kThreads - kSmThreads);
         bool finite = true;
         if (qok) {
           uint32_t rmax[4] = {0u, 0u, 0u, 0u};  // packed maxima of |bf16| bit patterns (NaN above inf)
@@ -499,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = (sm_tid >> 3) + 16 * r;
             finite &= amax < 0x7F80u || row >= p.H;
             int e = 0;
-            if (amax >= 0x4700u && amax < 0x7F80u) e = 14 - ((int)(amax >> 7) - 127);  // >= 2^15
+            if (amax >= 0x4700u && amax < 0x7F80u) e = 14 - ((int)(amax >> 7) - 127);       // >= 2^15
             else if (amax >= 0x0080u && amax < 0x3C80u) e = 14 - ((int)(amax >> 7) - 127);  // normal, < 2^-6
             else if (amax > 0u && amax < 0x0080u) e = 126;  // bf16 subnormals only
             if (row >= p.H) e = 0;  // rows of the next query (or beyond the tensor): not computed here
@@ -525,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w[uu] = *reinterpret_cast<const uint32_t*>(&b2);
                   }
                 }
-                *reinterpret_cast<uint4*>(sQ + b * kBlk + sw128_offset(row, 16 * chunk)) = v;
+                *reinterpret_cast<uint4*>(sQ + b * kQBlk + sw128_offset(row, 16 * chunk)) = v;
               }
             }
           }
@@ -541,20 +569,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l_part = 0.f;
 #pragma unroll 1
       for (int jt = ta; jt < tb; ++jt, ++i) {
-        const int s = i & 1;
-        const uint32_t ph = (uint32_t)(i >> 1) & 1u;
+        const int s = i & 3;
+        const uint32_t ph = (uint32_t)(i >> 2) & 1u;
         // every exit decision is taken by all four softmax warps together (no partial barriers)
-        // (the last block barrier also orders the producers' row-validity bytes before the reads below)
+        // (the RoPE block barrier also orders the producers' row-validity bytes before the reads below)
         bool w = !*abort_flag && warp_wait(&s_full[s], ph, p.err, lane) &&
-                 warp_wait(&full[s * kBlocks + kBlocks - 1], ph, p.err, lane);
+                 warp_wait(&full[s], ph, p.err, lane);
         if (named_bar_or(1, kSmThreads, !w)) {
           ok = false;
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        uint32_t xr[32];
-        tmem_ld16x2_32(tmem + lane_base + kColS + 64 * s, xr);
+        uint32_t xr[16];
+        tmem_ld16x2_16(tmem + lane_base + kColS + kRows * s, xr);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -562,19 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // logits in log2 units, in place (as float bits); masked rows become -inf
         float mt = -INFINITY;
         {
-          const uint4* vld4 = reinterpret_cast<const uint4*>(sValid + s * kRows + 32 * half);
+          const uint4 vv = *reinterpret_cast<const uint4*>(sValid + s * kRows + 16 * half);
+          const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-          for (int q4 = 0; q4 < 2; ++q4) {
-            const uint4 vv = vld4[q4];
-            const uint32_t w4[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              const int col = q4 * 16 + c;
-              const bool valid = (w4[c >> 2] >> (8 * (c & 3))) & 0xFFu;
-              const float v = valid ? __uint_as_float(xr[col]) * sc_log2 : -INFINITY;
-              xr[col] = __float_as_uint(v);
-              mt = fmaxf(mt, v);
-            }
+          for (int c = 0; c < 16; ++c) {
+            const bool valid = (w4[c >> 2] >> (8 * (c & 3))) & 0xFFu;
+            const float v = valid ? __uint_as_float(xr[c]) * sc_log2 : -INFINITY;
+            xr[c] = __float_as_uint(v);
+            mt = fmaxf(mt, v);
           }
         }
         mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
@@ -586,12 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_part *= alpha;
         m_ref = m_new;
         {
-          // P goes into this stage's RoPE block: QK of the tile has finished reading it (s_full), and
-          // the stage is not rewritten before PV of the tile releases it
+          // P goes into this stage's RoPE block as [head][32 rows] fp16 (64-byte rows, 64-byte
+          // swizzle): QK of the tile has finished reading the block (s_full), and the producers do
+          // not refill it before PV of the tile releases it. This thread writes rows 16 half ..
+          // 16 half + 15 of head h: two 16-byte chunks.
           uint8_t* sPt = sStage + s * kStageBytes + 8 * kBlk;
           float psum = 0.f;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
+          for (int ch = 0; ch < 2; ++ch) {
             uint32_t pk[4];
 #pragma unroll
             for (int uu = 0; uu < 4; ++uu) {
@@ -603,18 +628,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const __half2 h2 = __floats2half2_rn(p0, p1);
               pk[uu] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            *reinterpret_cast<uint4*>(sPt + sw128_offset(h, (4 * half + ch) * 16)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(sPt + sw64_offset(h, (2 * half + ch) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
           l_part += psum;
         }
-        // PV of the previous tile must have finished accumulating into O^T before it is rescaled and
-        // before this tile's PV is released. Waiting on every tile (after P is written: P is double
-        // buffered with the stages, so this costs no overlap) keeps this warp at most one phase
-        // behind the barrier, which its parity-based wait requires.
-        if (i > 0 && !warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane)) *abort_flag = 1;
-        // rescale O^T columns of the heads whose reference max moved (after P: fewer live registers)
+        // rescale O^T columns of the heads whose reference max moved, once PV of the previous tile
+        // (and so every earlier one: they complete in order) has finished accumulating into it
         if (any) {
+          if (!wait_pv(i - 1)) *abort_flag = 1;
           if (half == 0) sAlpha[h] = alpha;
           named_bar(1, kSmThreads);
           tc_fence_after();
@@ -631,33 +652,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // P and the corrected O^T are ready once all four warps are here; so is O^T of the previous
-        // query, read out by every warp before its first arrival for this one
+        // P (and the corrected O^T) of this warp are ready; the PV warp waits for all four
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0 && arrive_last(p_count)) {
-          // O^T += V^T . P^T: the stage read MN-major as A (M = 128 dims x4), P^T as B (N = 64 heads)
-          tc_fence_after();
-          const uint32_t sa = st_addr + (uint32_t)(s * kStageBytes);
-          const uint32_t p_addr = sa + 8 * kBlk;  // P of this tile in the stage's RoPE block
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = smem_desc(sa + (uint32_t)(2 * mt * kBlk + kk * 2048), kBlk, 1024, 2);
-              const uint64_t b = smem_desc(p_addr + kk * 32, 16, 1024, 2);
-              mma_bf16_ss(tmem + kColO + 64 * mt, a, b, idesc_pv, (jt > ta || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&empty[s * kEmpty + mt]);  // dim blocks 2mt, 2mt+1 may be refilled
-          }
-          mma_commit(pv_done);
-          mma_commit(&empty[s * kEmpty + 4]);     // P (the RoPE block) consumed
-        }
+        if (lane == 0) mbar_arrive(&p_ready[s]);
       }
       // ---- the query's normalisation and output (final, or a partial for the merge) ----
       if (ok) {
-        const bool w = warp_wait(pv_done, (uint32_t)(i - 1) & 1u, p.err, lane);
+        const bool w = wait_pv(i - 1);
         if (named_bar_or(1, kSmThreads, !w)) {
           ok = false;
           *abort_flag = 1;
@@ -705,12 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // O^T is read out before this warp's first P arrival of the next query lets PV overwrite it
+        tc_fence_before();
       }
-    }
-    // the PV MMAs this warp issued have completed before TMEM is released
-    if (lane == 0) {
-      mma_commit(pv_drain);
-      mbar_wait(pv_drain, 0, p.err);
     }
   }
   __syncthreads();
