@@ -595,7 +595,7 @@ def run_long_prefill_pass(args):
     peaks, peaks_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
     bf16 = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
-    fp8m = measure_fp8_peak() if rank == 0 else None
+    fp8m = measure_fp8_peak() if (rank == 0 and not args.no_peak) else None
     if fp8m and "fp8_tflops_sustained" in fp8m:
         fp8, fp8_src = fp8m["fp8_tflops_sustained"], "measured in this run (sustained e4m3 GEMM)"
     else:
@@ -603,7 +603,9 @@ def run_long_prefill_pass(args):
     pk = {"hbm": hbm, "fp8": fp8, "bf16": bf16}
 
     t0 = time.perf_counter()
-    chunks = inputs.config4_pass(seed=rank_seed(4, rank))
+    only = sorted(set(int(c) for c in args.chunks.split(","))) if args.chunks else None
+    chunks = inputs.config4_pass(seed=rank_seed(4, rank), chunks=only)
+    chunk_ids = only if only else list(range(len(chunks)))
     gen_s = time.perf_counter() - t0
     n, T = len(chunks), chunks[0].T
     total_tokens = n * T
@@ -725,12 +727,12 @@ def run_long_prefill_pass(args):
     roof["kernel"] = dom
     roof["achieved_over"] = "the kernel's 64 launches of one pass: algorithmic work / summed launch time"
     roof["peak_source"] = ("HBM and bf16 %s (MEASURED_PEAKS.json); e4m3 %s" % (peaks_kind, fp8_src))
-    tr = recorded_traffic(dom, "long-prefill-chunk63")
+    tr = recorded_traffic(dom, "long-prefill-chunk63") if chunk_ids[-1] == 63 else None
     roof["traffic"] = tr
     if tr is not None:
         roof["traffic_launch"] = "chunk 63 (2048 queries over up to 131,072 keys), one launch"
         roof["algorithmic_bytes_launch"] = works[-1][dom].bytes
-    curve = [{"chunk": c, "ctx_end": int((c + 1) * T), "indexer_ms": round(float(per[c, 0]), 4),
+    curve = [{"chunk": chunk_ids[c], "ctx_end": int((chunk_ids[c] + 1) * T), "indexer_ms": round(float(per[c, 0]), 4),
               "topk_ms": round(float(per[c, 1]), 4), "mla_ms": round(float(per[c, 2]), 4),
               "indexer_tflops": round(works[c]["indexer"].flops / (per[c, 0] * 1e9), 1),
               "mla_gbs": round(works[c]["mla"].bytes / (per[c, 2] * 1e6), 1)} for c in range(n)]
@@ -746,7 +748,7 @@ def run_long_prefill_pass(args):
 
     # ---- CPU baseline: the oracle on a stratified sample of the pass
     cpu = None
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and only is None:
         import oracle
         threads = oracle.num_threads(0)
         ntok, wall_cpu = long_prefill_cpu_sample(chunks)
@@ -759,7 +761,8 @@ def run_long_prefill_pass(args):
             "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3+bf16",
             "data": "synthetic",
-            "config": {"workload": "long-prefill-128K", "sequence_tokens": total_tokens, "chunks": n,
+            "config": {"workload": "long-prefill-128K" if only is None else "long-prefill-chunks-" + args.chunks,
+                       "sequence_tokens": total_tokens, "chunks": n,
                        "chunk_tokens": T, "index_heads": chunks[0].Hi, "index_dim": chunks[0].Di,
                        "topk": chunks[0].topk, "mla_heads": chunks[0].H, "page": 64,
                        "step": "one whole pass: 64 chunks x (indexer, top-k, sparse MLA)",
@@ -873,7 +876,7 @@ def run_hisparse(args):
     torch.cuda.set_device(0)
     hs.load()
     t0 = time.perf_counter()
-    hw = inputs.config5(steps=args.hisparse_steps, host_alloc=pinned_uint8)
+    hw = inputs.config5(B=args.hisparse_requests, steps=args.hisparse_steps, host_alloc=pinned_uint8)
     gen_s = time.perf_counter() - t0
     dh = DeviceHiSparse(hw)
     stream = torch.cuda.current_stream()
@@ -899,6 +902,19 @@ def run_hisparse(args):
     cnt = torch.stack(counters).cpu().numpy()          # [steps, 3] resident, hit, miss
     t_res = np.array([e[0].elapsed_time(e[1]) for e in ev])
     t_mla = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    # the host link's measured rate: one 1 GiB copy-engine copy from pinned host memory, best of 5
+    src = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    best = float("inf")
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    link_gbs = (1 << 30) / (best * 1e6)
+    del src, dst
     warm = slice(1, steps)
     miss_bytes = cnt[:, 2].astype(np.float64) * 656
     mla_w = cm.mla_work(hw.H, hw.B * hw.k, hw.B)
@@ -910,6 +926,12 @@ def run_hisparse(args):
             "step0_cold": {"resolve_ms": round(float(t_res[0]), 4), "mla_ms": round(float(t_mla[0]), 4),
                            "misses": int(cnt[0, 2]), "host_read_gbs": round(miss_bytes[0] / (t_res[0] * 1e6), 1)},
             "resolve_ms_steps": [round(float(x), 3) for x in t_res[:12]],
+            "resolve_ms_warm_p50": round(float(np.percentile(t_res[warm], 50)), 4),
+            "resolve_ms_warm_p95": round(float(np.percentile(t_res[warm], 95)), 4),
+            "host_link": {"copy_engine_h2d_gbs": round(link_gbs, 1),
+                          "how": "one 1 GiB copy from pinned host memory to the device, best of 5",
+                          "resolve_frac_warm": round(float((miss_bytes[warm] / (t_res[warm] * 1e6)).mean()) / link_gbs, 4),
+                          "resolve_frac_step0": round(miss_bytes[0] / (t_res[0] * 1e6) / link_gbs, 4)},
             "per_step_warm": {"hits": round(float(cnt[warm, 1].mean()), 1), "misses": round(float(cnt[warm, 2].mean()), 1),
                               "resident": round(float(cnt[warm, 0].mean()), 1),
                               "host_read_gbs": round(float((miss_bytes[warm] / (t_res[warm] * 1e6)).mean()), 1)},
@@ -983,8 +1005,11 @@ def main(argv=None):
     ap.add_argument("--requests", type=int, default=64, help="decode batch size (profiling runs use fewer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="--config 4: skip the MTP-decode and chunked-prefill keys")
+    ap.add_argument("--chunks", default="", help="--config 4: run only these chunks of the pass (comma list; profiling)")
+    ap.add_argument("--no-peak", action="store_true", help="--config 4: skip the e4m3 GEMM peak measurement (profiling)")
     ap.add_argument("--reps", type=int, default=5, help="--kv-append / --kv-offload: timed launches")
     ap.add_argument("--hisparse-steps", type=int, default=50, help="--config 5: decode steps")
+    ap.add_argument("--hisparse-requests", type=int, default=32, help="--config 5: requests (profiling runs use fewer)")
     ap.add_argument("--kv-append", type=int, default=0, help="time hs_kv_append on this many new tokens instead")
     ap.add_argument("--kv-offload", type=int, default=0, help="time hs_kv_offload on about this many pages instead")
     ap.add_argument("--shared-sets", action="store_true",
