@@ -39,3 +39,19 @@ def test_hisparse_stream_overlap_and_order():
             assert np.all(np.diff(row) > 0) and row[0] >= 0 and row[-1] < seq[r] - 4096
         for st in range(1, 5):
             assert len(np.intersect1d(s[st, r], s[st - 1, r])) == round(0.8 * 256)
+
+
+def test_long_prefill_pass_chunks_equal_single_chunk_builds():
+    """config4_pass builds the cache once and each chunk's queries from the chunk's own stream:
+    every chunk is byte for byte the workload config4 builds for that chunk alone, and different
+    chunks have different query values."""
+    kw = dict(total=4096, chunk_len=512, Hi=8, Di=64, H=4, topk=64)
+    ws = inputs.config4_pass(chunks=[0, 3, 7], **kw)
+    for c, w in zip([0, 3, 7], ws):
+        one = inputs.config4(c, **kw)
+        for f in ("q_idx", "q_scale", "weights", "q_mla", "token_kvlen", "token_req", "k_cache", "k_scale",
+                  "block_table", "kv_pool"):
+            assert np.array_equal(getattr(w, f), getattr(one, f)), (c, f)
+        assert w.token_kvlen.tolist() == list(range(512 * c + 1, 512 * c + 513))
+    assert not np.array_equal(ws[0].q_mla, ws[1].q_mla)
+    assert ws[1].kv_pool is ws[0].kv_pool          # the cache is shared, not copied
