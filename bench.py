@@ -662,22 +662,29 @@ def run_long_prefill_pass(args):
     in_ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
+    # timing events of each chunk's copies, to report the achieved copy rates
+    t_in = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    t_out = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
 
     def copy_in(c):
         st = c & 1
         with torch.cuda.stream(cin):
             if c >= 2:
                 cin.wait_event(done[st])          # chunk c - 2 has finished reading this set
+            t_in[c][0].record(cin)
             for dst, h in zip(d_in[st], h_in[c]):
                 dst.copy_(h, non_blocking=True)
+            t_in[c][1].record(cin)
             in_ready[st].record(cin)
 
     def copy_out(c):
         st = c & 1
         with torch.cuda.stream(cout):
             cout.wait_event(done[st])
+            t_out[c][0].record(cout)
             h_out[c][0].copy_(d_out[st][0], non_blocking=True)
             h_out[c][1].copy_(d_out[st][1], non_blocking=True)
+            t_out[c][1].record(cout)
             out_done[st].record(cout)
 
     e2e_t = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -705,6 +712,8 @@ def run_long_prefill_pass(args):
     torch.cuda.synchronize()
     assert torch.equal(h_out[n - 1][0].view(torch.int16), lp.out[n - 1].cpu().view(torch.int16)), "e2e outputs differ"
     ms_e2e = max_over_ranks(e2e_t[0].elapsed_time(e2e_t[1]), world, dev)
+    ms_in = sum(a.elapsed_time(b) for a, b in t_in)
+    ms_out = sum(a.elapsed_time(b) for a, b in t_out)
     clk = clocks.stop() if rank == 0 else None
     del h_in, h_out, d_in, d_out
 
@@ -777,6 +786,11 @@ def run_long_prefill_pass(args):
             "other_workloads": others,
             "e2e": {"value": round(total_tokens * world / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4), "steps": 1,
+                    "copies": {"h2d_ms": round(ms_in, 2), "d2h_ms": round(ms_out, 2),
+                               "h2d_gbs": round(h2d / (ms_in * 1e6), 1), "d2h_gbs": round(d2h / (ms_out * 1e6), 1),
+                               "note": "summed durations of the chunks' copies on their own streams (they overlap "
+                                       "the kernels, so a sum above ms_per_step of the device pass means the "
+                                       "pass is copy-bound)"},
                     "overlap": "chunk c+1's inputs in and chunk c-1's outputs out on two copy streams while chunk c "
                                "computes (two device buffer sets)"},
             "gpu_launches": 3 * n * K, "cpu_baseline": cpu, "clocks": clk, "wall_s_timed_region": round(wall, 3),
