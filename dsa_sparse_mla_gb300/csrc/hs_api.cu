@@ -153,7 +153,7 @@ hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream) {
   if (a->T == 0) return ok();
   REQUIRE(a->q && a->kv_pool && a->idx && a->out, "a required pointer is NULL");
   REQUIRE(aligned16(a->q) && aligned16(a->kv_pool), "q and kv_pool must be 16-byte aligned");
-  REQUIRE(a->R >= 1, "R must be >= 1");
+  REQUIRE(a->R >= 1 && a->R <= INT32_MAX, "R must be in [1, 2^31 - 1]");
   REQUIRE(!a->block_table || (a->token_req && a->bt_stride >= 1), "block_table needs token_req and bt_stride >= 1");
   REQUIRE(!a->idx_row || a->idx_rows >= 1, "idx_row needs idx_rows >= 1");
   REQUIRE(!a->token_kvlen || a->block_table, "token_kvlen needs block_table (it limits logical token indices)");

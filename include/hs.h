@@ -201,7 +201,7 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  *   T, H          query tokens; heads, 1 <= H <= 64
  *   k             entries per idx row
  *   q             bf16 [T, H, 576] (16-byte aligned)
- *   kv_pool       uint8 [R, 656] (16-byte aligned)
+ *   kv_pool       uint8 [R, 656] (16-byte aligned), 1 <= R <= 2^31 - 1 rows
  *   idx           int32 [T, k], or [idx_rows, k] with idx_row
  *   block_table   int32 [B, bt_stride] or NULL; token_req int32 [T] (required with block_table)
  *   idx_row       int32 [T] or NULL; idx_rows >= 1 rows of idx when given
@@ -212,7 +212,7 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  *                 bytes of 16-byte aligned device memory (contents need no initialisation, and are
  *                 scratch after the call): when one CTA per query would leave more than a quarter
  *                 of the SMs' time idle (fewer queries than SMs, or a mostly empty last wave), the
- *                 call gives every SM an equal share of the (query, 64-row tile) work instead. A query split between SMs leaves per-SM
+ *                 call gives every SM an equal share of the (query, 128-row tile) work instead. A query split between SMs leaves per-SM
  *                 partial results (softmax-normalised bf16 output and log-sum-exp) in the workspace,
  *                 which a second kernel on the same stream merges by log-sum-exp, as in [P1]
  *                 「DCP: KVキャッシュもシャーディング」 (partial attention merged across shards). Calls that
