@@ -613,9 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax / epilogue ========
     // S^T of a 64-row tile sits in the 64-row TMEM layout: tile row 16 q + r (q = the warp's lane
     // quarter, r < 16) in lane 32 q + r. Thread (warp w, lane l) owns row 16 (w % 4) + (l % 16) and
-    // heads hb .. hb + 31, hb = 32 (l / 16), read in groups of 16 (TMEM 16x32bx2 loads, the second
-    // half-warp 32 columns further on), so that only 16 logits are held at a time: once for the
-    // threshold check, once for P, and a third time when the maxima move.
+    // heads hb .. hb + 31, hb = 32 (l / 16), read with one TMEM 16x32bx2 load per tile (the second
+    // half-warp 32 columns further on) and kept in registers for the check, the maxima and P.
     const int quad = warp & 3;            // TMEM lane quarter this warp may access
     const int row = quad * 16 + (lane & 15);
     const int hb = 32 * (lane >> 4);
@@ -736,21 +735,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const bool valid = sValid[s * kRows + row] != 0;
+        // this row's 32 logits, in one TMEM load (the second half-warp's columns are 32 further on)
+        uint32_t x[32];
+        tmem_ld16x2_32(s_col, x);
+        tmem_wait_ld();
+        // S^T has been read: QK of the tile after next may overwrite this buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[s]);
         // does a logit of this row exceed its head's reference max by more than the threshold?
         bool need = false;
-        {
+        if (valid) {
           const float* thr = sThr + 64 * v + hb;
 #pragma unroll
-          for (int gq = 0; gq < 2; ++gq) {
-            uint32_t x[16];
-            tmem_ld16x2_16_o32(s_col + 16 * gq, x);
-            tmem_wait_ld();
-            if (valid) {
-#pragma unroll
-              for (int c = 0; c < 16; ++c)
-                need |= __uint_as_float(x[c]) * cof(hb + 16 * gq + c) > thr[16 * gq + c];
-            }
-          }
+          for (int c = 0; c < 32; ++c) need |= __uint_as_float(x[c]) * cof(hb + c) > thr[c];
         }
         const bool moved = named_bar_or(1, kSmThreads, need);
         if (moved) {
@@ -758,15 +756,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // within each half-warp (lane l ends with heads hb + l % 16 and hb + 16 + l % 16), then
           // over the four warps
           float mx[16];
+          {
+            // first butterfly step straight from the logits (see half_transpose_pair_step)
+            const bool up = (lane & 1) != 0;
 #pragma unroll
-          for (int gq = 0; gq < 2; ++gq) {
-            uint32_t x[16];
-            tmem_ld16x2_16_o32(s_col + 16 * gq, x);
-            tmem_wait_ld();
-            float xs[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) xs[c] = valid ? __uint_as_float(x[c]) * cof(hb + 16 * gq + c) : -INFINITY;
-            half_transpose_pair_step<true>(xs, mx, gq, lane);
+            for (int k2 = 0; k2 < 16; ++k2) {
+              const float a = valid ? __uint_as_float(x[2 * k2]) * cof(hb + 2 * k2) : -INFINITY;
+              const float b = valid ? __uint_as_float(x[2 * k2 + 1]) * cof(hb + 2 * k2 + 1) : -INFINITY;
+              const float got = __shfl_xor_sync(0xffffffffu, up ? a : b, 1);
+              mx[k2] = fmaxf(up ? b : a, got);
+            }
           }
           half_transpose_finish<true>(mx, lane);
           sRed[quad * 64 + hb + (lane & 15)] = mx[0];
@@ -793,39 +792,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P = 2^(logit - max) as fp16 into the slot's RoPE block as [row][64 heads] (128-byte rows,
         // 128-byte swizzle): QK of the tile has finished reading the block (s_full), and the
-        // producers do not refill it before PV of the tile releases it. Each group of 16 heads is
-        // two 16-byte chunks.
+        // producers do not refill it before PV of the tile releases it. This thread's 32 heads are
+        // four 16-byte chunks.
         {
           const float* me = sMe + 64 * v + hb;
           uint8_t* sP = sTile + s * kTileBytes + 8 * kBlk;
+          uint32_t pk[16];
 #pragma unroll
-          for (int gq = 0; gq < 2; ++gq) {
-            uint32_t x[16];
-            tmem_ld16x2_16_o32(s_col + 16 * gq, x);
-            tmem_wait_ld();
-            uint32_t pk[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int hc = 16 * gq + 2 * c;
-              float p0 = 0.f, p1 = 0.f;
-              if (valid) {
-                p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), cof(hb + hc), -me[hc]));
-                p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), cof(hb + hc + 1), -me[hc + 1]));
-              }
-              l[hc] += p0;
-              l[hc + 1] += p1;
-              pk[c] = pack_half2(p0, p1);
+          for (int c = 0; c < 16; ++c) {
+            float p0 = 0.f, p1 = 0.f;
+            if (valid) {
+              p0 = fast_exp2(fmaf(__uint_as_float(x[2 * c]), cof(hb + 2 * c), -me[2 * c]));
+              p1 = fast_exp2(fmaf(__uint_as_float(x[2 * c + 1]), cof(hb + 2 * c + 1), -me[2 * c + 1]));
             }
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj)
-              *reinterpret_cast<uint4*>(sP + sw128_offset(row, 2 * hb + 32 * gq + 16 * jj)) =
-                  make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
+            l[2 * c] += p0;
+            l[2 * c + 1] += p1;
+            pk[c] = pack_half2(p0, p1);
           }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            *reinterpret_cast<uint4*>(sP + sw128_offset(row, 2 * hb + 16 * jj)) =
+                make_uint4(pk[4 * jj], pk[4 * jj + 1], pk[4 * jj + 2], pk[4 * jj + 3]);
         }
-        // S^T has been read: QK of the tile after next may overwrite this buffer
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[s]);
         // rescale O^T's columns (this warp's 32 dims of each M-tile) when the maxima moved, once PV
         // of the previous tile (and so every earlier one: they complete in order) has finished
         if (moved && jt > ta) {
