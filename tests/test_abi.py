@@ -58,6 +58,9 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1 and b"idx_rows" in L.hs_last_error()
     m.idx_row, m.token_kvlen = None, 16                               # a causal limit without a block table
     assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1 and b"token_kvlen needs" in L.hs_last_error()
+    m.token_kvlen, m.R = None, 2 ** 31                                # the gather keeps rows as int32
+    assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1 and b"R must be" in L.hs_last_error()
+    m.R = 1
     n = ctypes.c_uint64(0)
     assert L.hs_sparse_mla_workspace_size(0, ctypes.byref(n)) == 1 and b"H must be" in L.hs_last_error()
     r = hs._ResolveArgs()
