@@ -212,7 +212,7 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
  *                 bytes of 16-byte aligned device memory (contents need no initialisation, and are
  *                 scratch after the call): when one CTA per query would leave more than a quarter
  *                 of the SMs' time idle (fewer queries than SMs, or a mostly empty last wave), the
- *                 call gives every SM an equal share of the (query, 128-row tile) work instead. A query split between SMs leaves per-SM
+ *                 call gives every SM an equal share of the (query, 64-row tile) work instead. A query split between SMs leaves per-SM
  *                 partial results (softmax-normalised bf16 output and log-sum-exp) in the workspace,
  *                 which a second kernel on the same stream merges by log-sum-exp, as in [P1]
  *                 「DCP: KVキャッシュもシャーディング」 (partial attention merged across shards). Calls that
