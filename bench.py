@@ -248,7 +248,9 @@ def run_ours(args):
     w = build_workload(args.config, rank_seed(args.config, rank), args.requests)
     dw = DeviceWorkload.from_host(w, dev)
     Path = SharedSetHotPath if args.shared_sets else HotPath
-    hp = Path(dw)
+    # decode batches (the MTP-decode workload) run indexer and top-k as the one call hs_indexer_topk
+    fused = args.config == 2 and not args.separate
+    hp = Path(dw, fused=fused)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     work = work_of(w, args.shared_sets)
@@ -272,20 +274,46 @@ def run_ours(args):
         flush.fill_(i & 0xFF)
         e = ev[i]
         e[0].record(stream)
-        hp.indexer()
-        e[1].record(stream)
-        hp.topk()
-        e[2].record(stream)
+        if fused:
+            hp.indexer_topk()
+            e[1].record(stream)
+            e[2].record(stream)
+        else:
+            hp.indexer()
+            e[1].record(stream)
+            hp.topk()
+            e[2].record(stream)
         hp.mla()
         e[3].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(K)]
-    t_idx = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     t_mla = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
     ms_step = max_over_ranks(float(np.mean(t_step)), world, dev)
+    fused_info = None
+    if fused:
+        # the per-kernel split (and the roofline of each) from the same steps run as separate calls
+        t_it = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev2[i][0].record(stream)
+            hp.indexer()
+            ev2[i][1].record(stream)
+            hp.topk()
+            ev2[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_idx = [ev2[i][0].elapsed_time(ev2[i][1]) for i in range(K)]
+        t_topk = [ev2[i][1].elapsed_time(ev2[i][2]) for i in range(K)]
+        fused_info = {"indexer_topk_ms": round(float(np.mean(t_it)), 4),
+                      "separate_calls_ms": round(float(np.mean(t_idx)) + float(np.mean(t_topk)), 4),
+                      "note": "the step runs hs_indexer_topk (scores kept in L2 between the two kernels); "
+                              "kernels.indexer and kernels.topk come from the same steps run as the two "
+                              "separate calls"}
+    else:
+        t_idx = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+        t_topk = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     flag = hs.hs_check_flag(hp.err)
 
     # ---- end to end through host buffers (pinned), same API. Every step's inputs are copied in
@@ -296,7 +324,7 @@ def run_ours(args):
     names_in = ("q_idx", "q_scale", "weights", "q_mla", "token_req", "token_kvlen")
     h_in = [t.cpu().pin_memory() for t in hp.step_inputs()]
     dws = [dw, dataclasses.replace(dw, **{nm: torch.empty_like(getattr(dw, nm)) for nm in names_in})]
-    hps = [hp, Path(dws[1])]
+    hps = [hp, Path(dws[1], fused=fused)]
     h_out = [[torch.empty_like(hp.out, device="cpu").pin_memory(), torch.empty_like(hp.lse, device="cpu").pin_memory()]
              for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
@@ -418,11 +446,13 @@ def run_ours(args):
                        "ctx": "U{16384..65536}" if args.config == 2 else int(w.ctx.max()),
                        "index_heads": w.Hi, "index_dim": w.Di, "topk": w.topk, "mla_heads": w.H, "page": 64,
                        "l2": "256 MB write between timed steps (inputs also > L2)", "parallelism": "dp%d" % world,
+                       "indexer_topk": "one call (hs_indexer_topk)" if fused else "two calls",
                        "index_sets": ("shared: each request's final query token's top-k, reused by its other query "
                                       "tokens up to their own visible length") if args.shared_sets else "per query token"},
             "roofline": roof,
             "layer_roofline_frac": round(layer_roof_ms / tot, 4),
             "kernels": kern,
+            "indexer_topk_fused": fused_info,
             "e2e": {"value": round(tokens / (ms_e2e * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 4), "steps": K2,
                     "overlap": "inputs of step i+1 in and outputs of step i-1 out on a second stream during step i "
@@ -503,13 +533,15 @@ def kernel_rooflines(works, ms, hbm, fp8, bf16):
     return out
 
 
-def measure_hot_path(w, steps: int, warmup: int, dev, peaks):
+def measure_hot_path(w, steps: int, warmup: int, dev, peaks, fused: bool = False):
     """One workload's step (indexer -> top-k -> sparse MLA on all its query tokens): mean time per
-    step and per kernel over `steps` timed steps, a 256 MB L2 flush before each."""
+    step and per kernel over `steps` timed steps, a 256 MB L2 flush before each. With `fused`
+    (decode batches) the step's value is also measured with hs_indexer_topk in place of the two
+    calls."""
     import torch
     import dsa_sparse_mla_gb300 as hs
     from dsa_sparse_mla_gb300.pipeline import DeviceWorkload, HotPath
-    hp = HotPath(DeviceWorkload.from_host(w, dev))
+    hp = HotPath(DeviceWorkload.from_host(w, dev), fused=fused)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(warmup):
@@ -531,13 +563,30 @@ def measure_hot_path(w, steps: int, warmup: int, dev, peaks):
           for j, n in enumerate(("indexer", "topk", "mla"))}
     step_ms = float(np.mean([ev[i][0].elapsed_time(ev[i][3]) for i in range(steps)]))
     kern = kernel_rooflines([work_of(w)], ms, peaks["hbm"], peaks["fp8"], peaks["bf16"])
-    flag = hs.hs_check_flag(hp.err)
+    out = {"value": round(w.T / (step_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(step_ms, 4),
+           "steps": steps, "query_tokens": w.T, "kernels": kern,
+           "layer_roofline_frac": round(sum(k["roofline_ms"] for k in kern.values()) / sum(ms.values()), 4)}
+    if fused:
+        evf = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            evf[i][0].record(stream)
+            hp.indexer_topk()
+            evf[i][1].record(stream)
+            hp.mla()
+            evf[i][2].record(stream)
+        torch.cuda.synchronize()
+        f_step = float(np.mean([evf[i][0].elapsed_time(evf[i][2]) for i in range(steps)]))
+        f_it = float(np.mean([evf[i][0].elapsed_time(evf[i][1]) for i in range(steps)]))
+        out["indexer_topk_fused"] = {"value": round(w.T / (f_step * 1e-3), 1), "unit": "tokens/s",
+                                     "ms_per_step": round(f_step, 4), "indexer_topk_ms": round(f_it, 4),
+                                     "separate_calls_ms": round(ms["indexer"] + ms["topk"], 4),
+                                     "note": "the same step with hs_indexer_topk (scores kept in L2) in place "
+                                             "of hs_indexer_scores + hs_topk"}
+    out["device_flag"] = hs.hs_check_flag(hp.err)
     del hp, flush
     torch.cuda.empty_cache()
-    return {"value": round(w.T / (step_ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(step_ms, 4),
-            "steps": steps, "query_tokens": w.T, "kernels": kern,
-            "layer_roofline_frac": round(sum(k["roofline_ms"] for k in kern.values()) / sum(ms.values()), 4),
-            "device_flag": flag}
+    return out
 
 
 # ------------------------------------------------------------------------ analysis modes ----
@@ -752,7 +801,7 @@ def run_long_prefill_pass(args):
     if not args.no_extra:
         for cfg, steps in ((2, 200), (3, 20)):
             w = build_workload(cfg, rank_seed(cfg, 0))
-            others[w.name] = measure_hot_path(w, steps, 3, dev, pk)
+            others[w.name] = measure_hot_path(w, steps, 3, dev, pk, fused=cfg == 2)
             del w
 
     # ---- CPU baseline: the oracle on a stratified sample of the pass
@@ -1026,6 +1075,8 @@ def main(argv=None):
     ap.add_argument("--hisparse-requests", type=int, default=32, help="--config 5: requests (profiling runs use fewer)")
     ap.add_argument("--kv-append", type=int, default=0, help="time hs_kv_append on this many new tokens instead")
     ap.add_argument("--kv-offload", type=int, default=0, help="time hs_kv_offload on about this many pages instead")
+    ap.add_argument("--separate", action="store_true",
+                    help="--config 2: run indexer and top-k as two calls in the step, not hs_indexer_topk")
     ap.add_argument("--shared-sets", action="store_true",
                     help="the query tokens of a request share its final token's index set (indexer and top-k "
                          "run for final tokens only)")

@@ -14,6 +14,7 @@ import os
 import torch
 
 __all__ = ["HSError", "lib_path", "load", "hs_abi_version", "hs_check_flag", "hs_indexer_scores", "hs_topk",
+           "hs_indexer_topk",
            "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size", "hs_sparse_mla_fwd_static", "hs_hisparse_resolve",
            "hs_hisparse_touch_host", "hs_kv_append", "hs_kv_offload", "FLAGS"]
 
@@ -76,6 +77,7 @@ def load():
         lib.hs_check_flag.argtypes = [_P, _P, _P]
         lib.hs_indexer_scores.argtypes = [ctypes.POINTER(_IndexerArgs), _P]
         lib.hs_topk.argtypes = [_P, _i64, _P, _i32, _i32, _P, _P, _P]
+        lib.hs_indexer_topk.argtypes = [ctypes.POINTER(_IndexerArgs), _i32, _P, _P]
         lib.hs_sparse_mla_fwd.argtypes = [ctypes.POINTER(_MlaArgs), _P]
         lib.hs_sparse_mla_workspace_size.argtypes = [_i32, ctypes.POINTER(ctypes.c_uint64)]
         lib.hs_sparse_mla_fwd_static.argtypes = [ctypes.POINTER(_MlaArgs), _P]
@@ -83,7 +85,7 @@ def load():
         lib.hs_hisparse_touch_host.argtypes = [_i32, _P, _P, _P, _P, _P]
         lib.hs_kv_append.argtypes = [ctypes.POINTER(_AppendArgs), _P]
         lib.hs_kv_offload.argtypes = [ctypes.POINTER(_OffloadArgs), _P]
-        for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
+        for f in ("hs_check_flag", "hs_indexer_scores", "hs_topk", "hs_indexer_topk", "hs_sparse_mla_fwd", "hs_sparse_mla_workspace_size",
                   "hs_sparse_mla_fwd_static", "hs_hisparse_resolve", "hs_hisparse_touch_host", "hs_kv_append", "hs_kv_offload"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
@@ -129,20 +131,38 @@ def hs_check_flag(err_flag: torch.Tensor, stream=None) -> int:
     return int(out.value)
 
 
-def hs_indexer_scores(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, err_flag,
-                      num_requests: int | None = None, stream=None):
-    """Lightning-indexer scores into ``scores`` (float32 [T, ld]); see include/hs.h."""
+def _indexer_args(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, err_flag,
+                  num_requests):
     _dev(q, "q", torch.uint8), _dev(q_scale, "q_scale", torch.float32), _dev(weights, "weights", torch.float32)
     _dev(k_cache, "k_cache", torch.uint8), _dev(k_scale, "k_scale", torch.float32)
     _dev(block_table, "block_table", torch.int32), _dev(token_req, "token_req", torch.int32)
     _dev(token_kvlen, "token_kvlen", torch.int32), _dev(scores, "scores", torch.float32)
     _dev(err_flag, "err_flag", torch.int32)
     T, Hi, Di = q.shape
-    a = _IndexerArgs(T, num_requests if num_requests is not None else block_table.shape[0], Hi, Di, _ptr(q),
-                     _ptr(q_scale), _ptr(weights), _ptr(k_cache), _ptr(k_scale), k_cache.shape[0],
-                     _ptr(block_table), block_table.shape[1], _ptr(token_req), _ptr(token_kvlen), _ptr(scores),
-                     scores.shape[1], _ptr(err_flag))
+    return _IndexerArgs(T, num_requests if num_requests is not None else block_table.shape[0], Hi, Di, _ptr(q),
+                        _ptr(q_scale), _ptr(weights), _ptr(k_cache), _ptr(k_scale), k_cache.shape[0],
+                        _ptr(block_table), block_table.shape[1], _ptr(token_req), _ptr(token_kvlen), _ptr(scores),
+                        scores.shape[1], _ptr(err_flag))
+
+
+def hs_indexer_scores(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, err_flag,
+                      num_requests: int | None = None, stream=None):
+    """Lightning-indexer scores into ``scores`` (float32 [T, ld]); see include/hs.h."""
+    a = _indexer_args(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, err_flag,
+                      num_requests)
     _check(load().hs_indexer_scores(ctypes.byref(a), _stream(stream)))
+
+
+def hs_indexer_topk(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, k: int, idx,
+                    err_flag, num_requests: int | None = None, stream=None):
+    """Indexer scores and their top-k in one call (``scores`` is scratch, undefined afterwards);
+    the indices go to ``idx`` (int32 [T, k]), as hs_indexer_scores + hs_topk would write them."""
+    a = _indexer_args(q, q_scale, weights, k_cache, k_scale, block_table, token_req, token_kvlen, scores, err_flag,
+                      num_requests)
+    _dev(idx, "idx", torch.int32)
+    if tuple(idx.shape) != (q.shape[0], k):
+        raise HSError(1, "idx must have shape [T, k]")
+    _check(load().hs_indexer_topk(ctypes.byref(a), k, _ptr(idx), _stream(stream)))
 
 
 def hs_topk(scores, token_kvlen, k: int, idx, err_flag, stream=None):

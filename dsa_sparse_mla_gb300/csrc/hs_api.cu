@@ -8,9 +8,10 @@
 #include "common.cuh"
 
 namespace hs {
-cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t stream, const char** why);
+cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, bool keep_scores, cudaStream_t stream,
+                           const char** why);
 cudaError_t launch_topk(const float* scores, int64_t ld, const int32_t* kvlen, int32_t T, int32_t k, int32_t* idx,
-                        int32_t* err, cudaStream_t stream);
+                        int32_t* err, bool discard, cudaStream_t stream);
 cudaError_t launch_mla(const hs_mla_args* a, int sms, cudaStream_t stream, const char** why);
 uint64_t mla_workspace_bytes(int32_t H, int sms);
 cudaError_t launch_resolve(const hs_resolve_args* a, cudaStream_t stream);
@@ -127,7 +128,7 @@ hs_status hs_indexer_scores(const hs_indexer_args* a, hs_stream_t stream) {
   hs_status st = check_device(&sms);
   if (st != HS_OK) return st;
   const char* why = nullptr;
-  return launched(hs::launch_indexer(a, sms, (cudaStream_t)stream, &why), "hs_indexer_scores", why);
+  return launched(hs::launch_indexer(a, sms, false, (cudaStream_t)stream, &why), "hs_indexer_scores", why);
 }
 
 hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, int32_t T, int32_t k, int32_t* idx,
@@ -140,8 +141,34 @@ hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, i
   REQUIRE(scores && token_kvlen && idx, "a required pointer is NULL");
   hs_status st = check_device(nullptr);
   if (st != HS_OK) return st;
-  return launched(hs::launch_topk(scores, ld, token_kvlen, T, k, idx, err_flag, (cudaStream_t)stream), "hs_topk",
+  return launched(hs::launch_topk(scores, ld, token_kvlen, T, k, idx, err_flag, false, (cudaStream_t)stream), "hs_topk",
                   nullptr);
+}
+
+hs_status hs_indexer_topk(const hs_indexer_args* a, int32_t k, int32_t* idx, hs_stream_t stream) {
+  REQUIRE(a, "args is NULL");
+  REQUIRE(a->T >= 0 && a->B >= 1, "need T >= 0 and B >= 1 (T=%d, B=%d)", a->T, a->B);
+  REQUIRE(a->Hi == 8 || a->Hi == 16 || a->Hi == 32 || a->Hi == 64, "Hi must be 8, 16, 32 or 64 (got %d)", a->Hi);
+  REQUIRE(a->Di == 64 || a->Di == 128, "Di must be 64 or 128 (got %d)", a->Di);
+  REQUIRE(k >= 1 && k <= 65536, "k must be in [1, 65536] (got %d)", k);
+  REQUIRE(a->err_flag, "err_flag is NULL");
+  if (a->T == 0) return ok();
+  REQUIRE(a->q && a->q_scale && a->weights && a->k_cache && a->k_scale && a->block_table && a->token_req &&
+              a->token_kvlen && a->scores && idx,
+          "a required pointer is NULL");
+  REQUIRE(aligned16(a->q) && aligned16(a->k_cache), "q and k_cache must be 16-byte aligned");
+  REQUIRE(a->nblk >= 1 && a->nblk * 64 <= INT32_MAX, "nblk out of range (%lld)", (long long)a->nblk);
+  REQUIRE(a->bt_stride >= 1 && a->ld >= 1, "bt_stride and ld must be >= 1");
+  REQUIRE((int64_t)a->T * a->Hi <= INT32_MAX, "T * Hi too large");
+  int sms = 0;
+  hs_status st = check_device(&sms);
+  if (st != HS_OK) return st;
+  const char* why = nullptr;
+  st = launched(hs::launch_indexer(a, sms, true, (cudaStream_t)stream, &why), "hs_indexer_topk (indexer)", why);
+  if (st != HS_OK) return st;
+  return launched(hs::launch_topk(a->scores, a->ld, a->token_kvlen, a->T, k, idx, a->err_flag, true,
+                                  (cudaStream_t)stream),
+                  "hs_indexer_topk (top-k)", nullptr);
 }
 
 hs_status hs_sparse_mla_fwd(const hs_mla_args* a, hs_stream_t stream) {

@@ -53,6 +53,7 @@ struct Params {
   int64_t ld;
   int32_t* err;
   int32_t scale_tma;  // k_scale is 16-byte aligned: the TMA warp copies each page's 64 scales to smem
+  int32_t keep_scores;  // keys and their scales are read evict-first and the scores stored evict-last in L2
 };
 
 // Work map: every CTA stages the launch's token lengths in chunks, derives each group's number
@@ -143,7 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<DI, HI>;
   constexpr int G = C::G;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned to 1024 bytes by pointer arithmetic on the shared array itself, so that the compiler
+  // still knows every pointer derived from it is a shared-memory one (shared loads and stores
+  // with 32-bit addresses, not generic ones)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
   float* sW = (float*)(smem + C::kOffW);                 // (w * q_scale) [G][HI] of the current group
@@ -378,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ------------------------------------------------------------ TMA producer ----------------
       if (lane == 0) {
+        const uint64_t pol_first = l2_policy_evict_first();
         if (new_group) {
           if (prev_g < 0) {
             prefetch_tensormap(&map_q);
@@ -403,10 +408,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(&full[st], bytes);
             for (int pg = 0; pg < 2; ++pg)
               if (blk[pg] >= 0) {
-                tma_load_2d(sK + st * C::kTileBytes + pg * 64 * DI, &map_k, &full[st], 0, blk[pg] * 64);
-                if (p.scale_tma)
-                  bulk_g2s(sScale + (it_prod % kScaleRing) * kBlockM + pg * 64, p.k_scale + (int64_t)blk[pg] * 64,
-                           64 * 4, &full[st]);
+                void* kdst = sK + st * C::kTileBytes + pg * 64 * DI;
+                float* sdst = sScale + (it_prod % kScaleRing) * kBlockM + pg * 64;
+                const float* ssrc = p.k_scale + (int64_t)blk[pg] * 64;
+                if (p.keep_scores) {
+                  tma_load_2d_hint(kdst, &map_k, &full[st], 0, blk[pg] * 64, pol_first);
+                  if (p.scale_tma) bulk_g2s_hint(sdst, ssrc, 64 * 4, &full[st], pol_first);
+                } else {
+                  tma_load_2d(kdst, &map_k, &full[st], 0, blk[pg] * 64);
+                  if (p.scale_tma) bulk_g2s(sdst, ssrc, 64 * 4, &full[st]);
+                }
               }
           }
         }
@@ -526,7 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int k = 0; k < kTok; ++k) {
                 const int g = c2 * kTok + k;
-                if (j < lim_s[g]) srow[(int64_t)g * p.ld + (int64_t)kt * kBlockM] = ks * sc[c2][k];
+                if (j < lim_s[g]) {
+                  float* dst = srow + (int64_t)g * p.ld + (int64_t)kt * kBlockM;
+                  if (p.keep_scores) st_global_hint(dst, ks * sc[c2][k], l2_policy_evict_last());
+                  else *dst = ks * sc[c2][k];
+                }
               }
           }
         }
@@ -573,7 +588,8 @@ static cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, Params
 }  // namespace indexer
 
 // Called by the C ABI after argument checks. Encodes the tensor maps and launches.
-cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t stream, const char** why) {
+cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, bool keep_scores, cudaStream_t stream,
+                           const char** why) {
   using namespace indexer;
   CUtensorMap mq, mk;
   const int DI = a->Di, HI = a->Hi;
@@ -605,6 +621,7 @@ cudaError_t launch_indexer(const hs_indexer_args* a, int num_sms, cudaStream_t s
   p.t_base = 0;
   p.ngroups = 0;
   p.scale_tma = ((uintptr_t)a->k_scale & 15) == 0 ? 1 : 0;
+  p.keep_scores = keep_scores ? 1 : 0;
   if (a->T == 0) return cudaSuccess;
   const int ctas = num_sms;  // persistent: one CTA per SM, each an equal share of the tiles
 #define HS_IDX_CASE(D, H) \

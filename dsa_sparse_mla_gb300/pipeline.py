@@ -2,7 +2,8 @@
 
 ``DeviceWorkload`` moves a seeded ``inputs.Workload`` into GPU memory; ``HotPath`` owns the
 intermediate and output buffers and runs one step: hs_indexer_scores -> hs_topk ->
-hs_sparse_mla_fwd (logical indices through the paged block table); ``SharedSetHotPath`` runs the
+hs_sparse_mla_fwd (logical indices through the paged block table), or for decode batches
+hs_indexer_topk -> hs_sparse_mla_fwd; ``SharedSetHotPath`` runs the
 indexer and top-k for each request's final query token only and lets the request's other query
 tokens reuse that set in hs_sparse_mla_fwd (shared index sets); ``LongPrefillPass`` runs every
 chunk of a long prefill through the same three calls. ``DeviceHiSparse`` does the
@@ -18,7 +19,7 @@ import dataclasses
 import numpy as np
 import torch
 
-from . import (hs_hisparse_resolve, hs_hisparse_touch_host, hs_indexer_scores, hs_sparse_mla_fwd,
+from . import (hs_hisparse_resolve, hs_hisparse_touch_host, hs_indexer_scores, hs_indexer_topk, hs_sparse_mla_fwd,
                hs_sparse_mla_workspace_size, hs_topk)
 from .inputs import HiSparseWorkload, Workload
 
@@ -53,12 +54,15 @@ class DeviceWorkload:
 
 
 class HotPath:
-    """Buffers and launches for one step of indexer -> top-k -> sparse MLA."""
+    """Buffers and launches for one step of indexer -> top-k -> sparse MLA. With ``fused`` (decode
+    batches) the step runs indexer and top-k as the one call hs_indexer_topk, whose scores stay in
+    L2 between the two kernels."""
 
-    def __init__(self, dw: DeviceWorkload):
+    def __init__(self, dw: DeviceWorkload, fused: bool = False):
         w = dw.w
         dev = dw.q_idx.device
         self.dw = dw
+        self.fused = fused
         self.scores = torch.empty((w.T, w.ld), dtype=torch.float32, device=dev)
         self.idx = torch.empty((w.T, w.topk), dtype=torch.int32, device=dev)
         self.out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
@@ -81,14 +85,22 @@ class HotPath:
     def topk(self, stream=None):
         hs_topk(self.scores, self.dw.token_kvlen, self.dw.w.topk, self.idx, self.err, stream=stream)
 
+    def indexer_topk(self, stream=None):
+        d = self.dw
+        hs_indexer_topk(d.q_idx, d.q_scale, d.weights, d.k_cache, d.k_scale, d.block_table, d.token_req,
+                        d.token_kvlen, self.scores, d.w.topk, self.idx, self.err, num_requests=d.w.B, stream=stream)
+
     def mla(self, stream=None):
         d = self.dw
         hs_sparse_mla_fwd(d.q_mla, d.kv_pool, self.idx, d.w.softmax_scale, self.out, self.err, lse=self.lse,
                           block_table=d.block_table, token_req=d.token_req, workspace=self.workspace, stream=stream)
 
     def step(self, stream=None):
-        self.indexer(stream)
-        self.topk(stream)
+        if self.fused:
+            self.indexer_topk(stream)
+        else:
+            self.indexer(stream)
+            self.topk(stream)
         self.mla(stream)
 
 
@@ -155,8 +167,8 @@ class SharedSetHotPath(HotPath):
     (idx_row), limited to the tokens it can see (token_kvlen), so MTP tokens do not re-run the
     indexer."""
 
-    def __init__(self, dw: DeviceWorkload):
-        super().__init__(dw)
+    def __init__(self, dw: DeviceWorkload, fused: bool = False):
+        super().__init__(dw, fused)
         w = dw.w
         dev = dw.q_idx.device
         req = np.asarray(w.token_req)
@@ -185,6 +197,12 @@ class SharedSetHotPath(HotPath):
 
     def topk(self, stream=None):
         hs_topk(self.scores, self.f_kvlen, self.dw.w.topk, self.idx, self.err, stream=stream)
+
+    def indexer_topk(self, stream=None):
+        d = self.dw
+        hs_indexer_topk(self.f_q_idx, self.f_q_scale, self.f_weights, d.k_cache, d.k_scale, d.block_table,
+                        self.f_req, self.f_kvlen, self.scores, d.w.topk, self.idx, self.err, num_requests=d.w.B,
+                        stream=stream)
 
     def mla(self, stream=None):
         d = self.dw

@@ -5,6 +5,7 @@
  *
  *   hs_indexer_scores   lightning-indexer scores of every visible prior token  (FP8 tcgen05 GEMM)
  *   hs_topk             per-query top-k of those scores, lowest index wins ties
+ *   hs_indexer_topk     the two in one call, the scores kept in L2 between them (decode)
  *   hs_sparse_mla_fwd   softmax attention of all heads over the selected latent-KV rows
  *   hs_hisparse_resolve serve each selected token from resident KV, the hot buffer (LRU),
  *                       or a copy from pinned host memory into an LRU slot
@@ -86,7 +87,7 @@ typedef enum {
 #define HS_D_LATENT 512          /* latent (value) width */
 #define HS_D_ROPE 64             /* RoPE width */
 #define HS_D_QK 576              /* query / key width = HS_D_LATENT + HS_D_ROPE */
-#define HS_ABI_VERSION 6
+#define HS_ABI_VERSION 7
 
 int hs_abi_version(void);
 const char* hs_status_str(hs_status s);
@@ -164,6 +165,27 @@ hs_status hs_indexer_scores(const hs_indexer_args* a, hs_stream_t stream);
  * ---------------------------------------------------------------------------------------- */
 hs_status hs_topk(const float* scores, int64_t ld, const int32_t* token_kvlen, int32_t T, int32_t k,
                   int32_t* idx, int32_t* err_flag, hs_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * hs_indexer_topk — indexer scores and their top-k in one call, the scores kept on chip.
+ *
+ * [P1] 「DP8とTP8が不十分な理由」: the indexer scores every prior token only so that top-k can
+ * pick 2,048 of them; the scores themselves are not needed afterwards. Same result as
+ * hs_indexer_scores(a) followed by hs_topk(a->scores, a->ld, a->token_kvlen, a->T, k, idx,
+ * a->err_flag): bit-identical idx. The difference is where the scores live between the two
+ * kernels: the indexer reads the keys and key scales under an L2 evict-first policy and stores
+ * the scores under evict-last, so that (when they fit beside the other live data of the L2,
+ * e.g. 256 MTP tokens x 64K keys = 64 MB of 129 MB) top-k reads them from L2, and top-k then
+ * drops each row's scores from L2 without writing them back. The scores do not go to HBM and
+ * back. Meant for decode batches, whose keys are read once per step; a prefill chunk reads its
+ * keys many times and should use the two calls.
+ *
+ *   a            as hs_indexer_scores; a->scores is scratch of the same shape [T, a->ld], whose
+ *                contents are undefined after the call
+ *   k, idx       as hs_topk: 1 <= k <= 65536; idx int32 [T, k] (output)
+ * Errors: as the two calls.
+ * ---------------------------------------------------------------------------------------- */
+hs_status hs_indexer_topk(const hs_indexer_args* a, int32_t k, int32_t* idx, hs_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * hs_sparse_mla_fwd — sparse MLA forward, MQA form (every KV row serves all heads).

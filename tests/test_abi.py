@@ -25,7 +25,7 @@ def lib():
 
 def test_header_declares_the_four_calls():
     names = _declared()
-    for n in ("hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_hisparse_resolve"):
+    for n in ("hs_indexer_scores", "hs_topk", "hs_sparse_mla_fwd", "hs_hisparse_resolve", "hs_indexer_topk"):
         assert n in names
 
 
@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert hs.hs_abi_version() == 6
+    assert hs.hs_abi_version() == 7
     hs.load()
     for code, name in enumerate(["HS_OK", "HS_ERR_INVALID", "HS_ERR_UNSUPPORTED", "HS_ERR_CUDA",
                                  "HS_ERR_DEVICE_FLAG", "HS_ERR_TIMEOUT"]):
@@ -50,6 +50,9 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     a = hs._IndexerArgs()
     a.T, a.B, a.Hi, a.Di = 4, 1, 12, 128                              # Hi = 12
     assert L.hs_indexer_scores(ctypes.byref(a), None) == 1 and b"Hi" in L.hs_last_error()
+    assert L.hs_indexer_topk(ctypes.byref(a), 2048, None, None) == 1 and b"Hi" in L.hs_last_error()
+    a.Hi = 64
+    assert L.hs_indexer_topk(ctypes.byref(a), 0, None, None) == 1 and b"k must be" in L.hs_last_error()
     m = hs._MlaArgs()
     m.T, m.H, m.k = 1, 0, 1
     assert L.hs_sparse_mla_fwd(ctypes.byref(m), None) == 1
