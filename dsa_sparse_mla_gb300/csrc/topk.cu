@@ -13,13 +13,14 @@
 // Fast path (one full pass over the row):
 //   sample: about 1/16 of the row (evenly spaced 128-score blocks) gives a key threshold tau that
 //           roughly 1.5 k scores of the row reach (adaptive histogram of the sample);
-//   filter: one pass appends the index of every score whose key is >= tau to its warp's region
-//           of a shared candidate list (ballots give the positions; keys are re-read later);
+//   filter: one pass appends the index and score of every score whose key is >= tau to its
+//           warp's region of a shared candidate list (ballots give the positions);
 //   select: an adaptive histogram of the candidates finds the bin holding the k-th largest; the
 //           few candidates in it are sorted by (key descending, index ascending), which fixes the
 //           exact composite threshold T; every candidate at or above T is kept;
-//   write:  kept indices are marked in a shared bitmap of the row, and a block-wide prefix sum of
-//           the bitmap's popcounts writes them in ascending order.
+//   write:  the candidate list is in index order already (warps own consecutive chunks and
+//           append in index order), so a ballot of the kept flags per 32 slots and a block-wide
+//           prefix sum of their popcounts give each kept index its output place.
 // The fast path gives up (and the exact path below runs) when the row has more than 262,144
 // scores, when the filter finds fewer than k candidates or more than 512 in one warp's chunk, or
 // when more than 1,024 candidates share the threshold bin.
@@ -48,11 +49,11 @@ constexpr int kSelBins = 4096;         // fast path: sample and candidate histog
 constexpr int kFastCand = kMaxCand * 2;  // fast path: candidate indices (uint32, same memory as cand)
 constexpr int kSample = 4096;          // fast path: sampled scores (at most)
 constexpr int kSmallSort = 1024;       // fast path: candidates of the threshold bin (at most)
-constexpr int kBitmapWords = 8192;     // fast path: rows of up to 262,144 scores
+constexpr int kFastMaxN = 262144;      // fast path: rows of up to this many scores
 constexpr int kOffCand = 0;                            // uint64 [kMaxCand] (sample keys alias it)
 constexpr int kOffHist = kOffCand + kMaxCand * 8;      // uint32 [kBins]
-constexpr int kOffBitmap = kOffHist + kBins * 4;       // uint32 [kBitmapWords] (+ small sort buffer)
-constexpr int kSmem = kOffBitmap + kBitmapWords * 4;
+constexpr int kOffCKey = kOffHist + kBins * 4;         // fast path: uint32 [kFastCand] candidate scores
+constexpr int kSmem = kOffCKey + kFastCand * 4;         // (the fast path's small sort buffer sits in hist)
 
 // Order-preserving key: x + 0 turns -0 into +0; negative numbers flip all bits, others the sign;
 // NaN maps to 0 (below every number).
@@ -129,8 +130,11 @@ __device__ __forceinline__ void walk_chunk_f(const float* row, int c0, int c1, b
   }
 }
 
-// Block-wide exclusive prefix sum of one value per thread; also returns the total.
+// Block-wide exclusive prefix sum of one value per thread; also returns the total. Each warp scans
+// its lanes, then every warp scans the sixteen warp totals itself (no second pass through shared
+// memory).
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* part, uint32_t& total) {
+  static_assert(kWarps <= 32, "one lane per warp total");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
@@ -140,47 +144,56 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* part, 
   }
   if (lane == 31) part[warp] = incl;
   __syncthreads();
-  uint32_t before = 0, all = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    const uint32_t x = part[w];
-    before += w < warp ? x : 0u;
-    all += x;
+  const uint32_t x = lane < kWarps ? part[lane] : 0u;
+  uint32_t xs = x;
+#pragma unroll
+  for (int o = 1; o < kWarps; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, xs, o);
+    if (lane >= o) xs += y;
   }
-  __syncthreads();
-  total = all;
+  const uint32_t before = __shfl_sync(0xffffffffu, xs - x, warp);
+  total = __shfl_sync(0xffffffffu, xs, kWarps - 1);
+  __syncthreads();  // part may be written again right after
   return before + incl - v;
 }
 
-// Over bins [0, nb) (nb <= kSelBins), finds the bin where the count accumulated from the top
-// reaches `need`: returns it with the count strictly above it (in *above) and its own count.
+// Over bins [0, nb) (nb <= kSelBins; every bin from nb up to kSelBins holds 0), finds the bin where
+// the count accumulated from the top reaches `need`: returns it with the count strictly above it
+// (in *above) and its own count. Thread t owns the eight bins NB - 8 - 8t .. NB - 1 - 8t (NB = nb
+// rounded up to 8), read with two 16-byte loads and visited from the top.
 __device__ __forceinline__ uint32_t bin_from_top(const uint32_t* hist, uint32_t nb, uint32_t need, uint32_t* part,
                                                  uint32_t* sh, uint32_t& above, uint32_t& count) {
-  constexpr int kPerT = kSelBins / kThreads;
+  static_assert(kSelBins == 8 * kThreads, "eight bins per thread");
   const int tid = threadIdx.x;
+  const int NB = (int)((nb + 7u) & ~7u);
+  const int base = NB - 8 - 8 * tid;  // lowest bin of this thread's eight
+  uint32_t c[8];
+  if (base >= 0) {
+    const uint4 a = *reinterpret_cast<const uint4*>(hist + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(hist + base + 4);
+    c[0] = b.w, c[1] = b.z, c[2] = b.y, c[3] = b.x, c[4] = a.w, c[5] = a.z, c[6] = a.y, c[7] = a.x;
+  } else {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) c[u] = 0u;
+  }
   uint32_t csum = 0;
 #pragma unroll
-  for (int u = 0; u < kPerT; ++u) {
-    const uint32_t rb = kPerT * tid + u;
-    csum += rb < nb ? hist[nb - 1 - rb] : 0u;
-  }
-  uint32_t total;
-  uint32_t run = block_excl_scan(csum, part, total);
-  if (tid == 0) {
+  for (int u = 0; u < 8; ++u) csum += c[u];
+  if (tid == 0) {  // ordered before the reads below by the scan's barriers
     sh[0] = 0xFFFFFFFFu;
     sh[1] = 0;
     sh[2] = 0;
   }
-  __syncthreads();
-#pragma unroll 1
-  for (int u = 0; u < kPerT; ++u) {
-    const uint32_t rb = kPerT * tid + u;
-    const uint32_t c = rb < nb ? hist[nb - 1 - rb] : 0u;
-    if (run < need && need <= run + c) {
-      sh[0] = nb - 1 - rb;
+  uint32_t total;
+  uint32_t run = block_excl_scan(csum, part, total);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (run < need && need <= run + c[u]) {
+      sh[0] = (uint32_t)(base + 7 - u);
       sh[1] = run;
-      sh[2] = c;
+      sh[2] = c[u];
     }
-    run += c;
+    run += c[u];
   }
   __syncthreads();
   above = sh[1];
@@ -200,11 +213,14 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
 // Candidates are score indices in per-warp regions of kFastCand / kWarps slots (the memory of the
 // exact path's candidate buffer); their keys are re-read from the row (L2) when needed.
 __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool vec, uint32_t* hist, uint32_t* cidx,
-                          uint32_t* bitmap, int32_t* out) {
+                          uint32_t* cscore, int32_t* out) {
   constexpr int kRegion = kFastCand / kWarps;  // candidate slots per warp
+  static_assert(kRegion == kThreads, "slot u * kRegion + t of the candidate list is thread t's u-th slot");
   __shared__ uint32_t part[kWarps], sh[4], f_min, f_max, f_small, f_valid, f_over, wcnt[kWarps];
+  __shared__ uint32_t kflag[kFastCand / 32], kbase[kFastCand / 32];  // kept flags and their prefix, per 32 slots
+  __shared__ uint64_t s_T;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (n > kBitmapWords * 32 || 3 * k > 2 * kFastCand / 2) return false;
+  if (n > kFastMaxN || 3 * k > 2 * kFastCand / 2) return false;
   // ---- sample: evenly spaced 128-score blocks, two per warp, loads issued together ----
   uint32_t* skeys = cidx;  // [kSample]
   const int nblk = (n + 127) / 128;
@@ -286,8 +302,6 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
     if (b == 0xFFFFFFFFu) return false;
     if (tid == 0) sh[3] = lo_s + (b << shift);
   }
-  const int words = (n + 31) / 32;
-  for (int i = tid; i < words; i += kThreads) bitmap[i] = 0;
   __syncthreads();
   const uint32_t tau = sh[3];
   // key >= tau  <=>  score >= ftau for every number (NaN fails both, its key being 0 < tau unless
@@ -295,25 +309,32 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
   const float ftau = key_to_float(tau);
   // ---- filter: the index of every score >= ftau goes to this warp's region ----
   uint32_t* region = cidx + kRegion * warp;
+  uint32_t* rscore = cscore + kRegion * warp;  // the candidates' scores (float bits), beside their indices
   uint32_t cnt = 0;  // candidates of this warp so far (warp-uniform)
   const uint32_t lt = (1u << lane) - 1u;
+  // Each lane counts its candidates of the step (0-4); three ballots of the count's bits give
+  // every lane its offset (lanes in order, each lane's candidates in index order). A step that
+  // would overflow the region stores nothing; the count still grows, and the overflow sends the
+  // row to the exact path.
   walk_chunk_f(row, c0, c1, vec, [&](int j0, const float (&x)[4], uint32_t valid) {
     uint32_t cm = 0;
 #pragma unroll
     for (int e = 0; e < 4; ++e) cm |= (x[e] >= ftau) ? (1u << e) : 0u;
     cm &= valid;
-    const uint32_t m0 = __ballot_sync(0xffffffffu, cm & 1u), m1 = __ballot_sync(0xffffffffu, cm & 2u);
-    const uint32_t m2 = __ballot_sync(0xffffffffu, cm & 4u), m3 = __ballot_sync(0xffffffffu, cm & 8u);
-    const uint32_t p0 = (uint32_t)__popc(m0), p1 = (uint32_t)__popc(m1), p2 = (uint32_t)__popc(m2);
-    uint32_t o = cnt + (uint32_t)__popc(m0 & lt);
-    if ((cm & 1u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0;
-    o = cnt + p0 + (uint32_t)__popc(m1 & lt);
-    if ((cm & 2u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0 + 1;
-    o = cnt + p0 + p1 + (uint32_t)__popc(m2 & lt);
-    if ((cm & 4u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0 + 2;
-    o = cnt + p0 + p1 + p2 + (uint32_t)__popc(m3 & lt);
-    if ((cm & 8u) && o < (uint32_t)kRegion) region[o] = (uint32_t)j0 + 3;
-    cnt += p0 + p1 + p2 + (uint32_t)__popc(m3);
+    const uint32_t c = (uint32_t)__popc(cm);
+    const uint32_t b0 = __ballot_sync(0xffffffffu, c & 1u), b1 = __ballot_sync(0xffffffffu, c & 2u);
+    const uint32_t b2 = __ballot_sync(0xffffffffu, c & 4u);
+    const uint32_t tot = (uint32_t)__popc(b0) + 2u * (uint32_t)__popc(b1) + 4u * (uint32_t)__popc(b2);
+    if (cnt + tot <= (uint32_t)kRegion) {  // warp-uniform
+      uint32_t o = cnt + (uint32_t)__popc(b0 & lt) + 2u * (uint32_t)__popc(b1 & lt) + 4u * (uint32_t)__popc(b2 & lt);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (cm & (1u << e)) {
+          region[o] = (uint32_t)j0 + e;
+          rscore[o++] = __float_as_uint(x[e]);
+        }
+    }
+    cnt += tot;
   });
   if (lane == 0) {
     wcnt[warp] = cnt;
@@ -324,21 +345,15 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
   const uint32_t C = f_valid - S;
   if (f_over || C < (uint32_t)k) return false;
   // ---- select: the k-th largest composite (key, -index) among the candidates ----
-  // Thread t owns slots t + 512 u (u < 16): their keys are loaded once, all loads in flight
-  // together, and kept in registers (0 marks an empty slot: no candidate has key 0, tau > 0).
+  // Thread t owns slots t + 512 u (u < 16): their keys, from the scores the filter stored, are
+  // kept in registers (0 marks an empty slot: no candidate has key 0, tau > 0).
   constexpr int kPer = kFastCand / kThreads;
   uint32_t ckey[kPer];
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const int i = tid + kThreads * u;
     const bool used = (uint32_t)(i % kRegion) < wcnt[i / kRegion];
-    ckey[u] = used ? __float_as_uint(__ldg(row + cidx[i])) : 0u;
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int i = tid + kThreads * u;
-    const bool used = (uint32_t)(i % kRegion) < wcnt[i / kRegion];
-    ckey[u] = used ? order_key(__uint_as_float(ckey[u])) : 0u;
+    ckey[u] = used ? order_key(__uint_as_float(cscore[i])) : 0u;
   }
   // Bins over [tau, sample max]; larger keys share the top bin (the map stays monotone, so the
   // selection stays exact: only the few candidates of the threshold bin are compared in full).
@@ -372,51 +387,70 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
         small[atomicAdd(&f_small, 1u)] = ((uint64_t)ckey[u] << 32) | (uint32_t)(0xFFFFFFFFu - j);
       }
     __syncthreads();
-    int P = 2;
-    while (P < (int)count) P <<= 1;
-    for (int i = (int)count + tid; i < P; i += kThreads) small[i] = 0;
-    __syncthreads();
-    // bitonic sort, descending
-    for (int size = 2; size <= P; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < (P >> 1); i += kThreads) {
-          const int a = 2 * stride * (i / stride) + (i % stride), c = a + stride;
-          const bool desc = (a & size) == 0;
-          const uint64_t x = small[a], y = small[c];
-          if ((x < y) == desc) {
-            small[a] = y;
-            small[c] = x;
-          }
-        }
-        __syncthreads();
+    const uint32_t want = (uint32_t)k - above - 1;  // rank of T within the bin, from the top
+    if (count <= 32) {
+      // one warp: each entry's rank is the number of larger entries (the composites are distinct)
+      if (warp == 0) {
+        const uint64_t v = lane < (int)count ? small[lane] : 0ull;
+        uint32_t r = 0;
+        for (int j = 0; j < (int)count; ++j) r += __shfl_sync(0xffffffffu, v, j) > v ? 1u : 0u;
+        if (lane < (int)count && r == want) s_T = v;
       }
+      __syncthreads();
+      T = s_T;
+    } else {
+      int P = 2;
+      while (P < (int)count) P <<= 1;
+      for (int i = (int)count + tid; i < P; i += kThreads) small[i] = 0;
+      __syncthreads();
+      // bitonic sort, descending
+      for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int i = tid; i < (P >> 1); i += kThreads) {
+            const int a = 2 * stride * (i / stride) + (i % stride), c = a + stride;
+            const bool desc = (a & size) == 0;
+            const uint64_t x = small[a], y = small[c];
+            if ((x < y) == desc) {
+              small[a] = y;
+              small[c] = x;
+            }
+          }
+          __syncthreads();
+        }
+      }
+      T = small[want];
     }
-    T = small[(uint32_t)k - above - 1];
   }
-  // ---- write: mark the kept candidates, then emit set bits in index order ----
+  // ---- write: the kept candidates in index order ----
+  // The candidate list is already in index order: region w before region w + 1 (the warps' chunks
+  // are consecutive) and ascending within a region. Slot (region u, position t) is thread t's
+  // u-th slot, so a ballot per region gives each warp's 32 kept flags as one word; an exclusive
+  // prefix over the 256 words in (region, word) order gives every kept candidate its output place.
+  uint32_t kept = 0;  // bit u: slot (u, tid) is kept
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const uint32_t j = cidx[tid + kThreads * u];
+    const bool kp = ckey[u] != 0u && ((((uint64_t)ckey[u] << 32) | (uint32_t)(0xFFFFFFFFu - j)) >= T);
+    kept |= kp ? 1u << u : 0u;
+    const uint32_t f = __ballot_sync(0xffffffffu, kp);
+    if (lane == 0) kflag[u * kWarps + warp] = f;
+  }
+  __syncthreads();
+  {
+    constexpr int kWords = kPer * kWarps;
+    static_assert(kWords <= kThreads, "one flag word per thread");
+    const uint32_t c = tid < kWords ? (uint32_t)__popc(kflag[tid]) : 0u;
+    uint32_t total;
+    const uint32_t before = block_excl_scan(c, part, total);
+    if (tid < kWords) kbase[tid] = before;
+  }
+  __syncthreads();
 #pragma unroll
   for (int u = 0; u < kPer; ++u)
-    if (ckey[u] != 0u) {
-      const uint32_t j = cidx[tid + kThreads * u];
-      if ((((uint64_t)ckey[u] << 32) | (uint32_t)(0xFFFFFFFFu - j)) >= T) atomicOr(&bitmap[j >> 5], 1u << (j & 31));
+    if ((kept >> u) & 1u) {
+      const uint32_t o = kbase[u * kWarps + warp] + (uint32_t)__popc(kflag[u * kWarps + warp] & lt);
+      if (o < (uint32_t)k) out[o] = (int32_t)cidx[tid + kThreads * u];
     }
-  __syncthreads();
-  const int wpt = (words + kThreads - 1) / kThreads;  // bitmap words per thread
-  const int w0 = tid * wpt;
-  const int w1 = w0 + wpt < words ? w0 + wpt : words;
-  uint32_t nset = 0;
-  for (int w = w0; w < w1; ++w) nset += (uint32_t)__popc(bitmap[w]);
-  uint32_t total;
-  uint32_t o = block_excl_scan(nset, part, total);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = bitmap[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1;
-      if (o < (uint32_t)k) out[o] = 32 * w + b;
-      ++o;
-    }
-  }
   return true;
 }
 
@@ -426,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem_raw + kOffHist);   // [kBins]
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem_raw + kOffCand);   // [kMaxCand]
-  uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + kOffBitmap);  // [kBitmapWords]
+  uint32_t* cscore = reinterpret_cast<uint32_t*>(smem_raw + kOffCKey);  // [kFastCand]
   __shared__ uint32_t red_min[kWarps], red_max[kWarps], warp_cnt[kWarps], warp_off[kWarps];
   __shared__ uint32_t scan_part[kWarps];
   __shared__ uint32_t sel_bin, sel_above, sel_count, n_cand;
@@ -453,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int c0 = warp * per;
     const int c1 = c0 + per < ni ? c0 + per : ni;
 
-    if (fast_topk(row, ni, k, c0, c1, vec, hist, reinterpret_cast<uint32_t*>(cand), bitmap, out)) return;
+    if (fast_topk(row, ni, k, c0, c1, vec, hist, reinterpret_cast<uint32_t*>(cand), cscore, out)) return;
 
     // ================================ exact path ==================================================
     // ---- pass 0: key range --------------------------------------------------------------------
