@@ -221,52 +221,55 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
   __shared__ uint64_t s_T;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (n > kFastMaxN || 3 * k > 2 * kFastCand / 2) return false;
-  // ---- sample: evenly spaced 128-score blocks, two per warp, loads issued together ----
-  uint32_t* skeys = cidx;  // [kSample]
+  // ---- sample: evenly spaced 128-score blocks, two per warp, loads issued together; the
+  // histogram is cleared while they are in flight, and each lane keeps its keys in registers ----
   const int nblk = (n + 127) / 128;
   const int sblk = nblk < kSample / 128 ? nblk : kSample / 128;
+  float4 v[2];
+  int jb[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int i = warp + kWarps * u;
+    jb[u] = i < sblk ? 128 * (i * nblk / sblk) : n;  // i * nblk < 2^16: 32-bit math
+    const int j0 = jb[u] + 4 * lane;
+    if (vec && j0 + 4 <= n) {
+      v[u] = __ldg(reinterpret_cast<const float4*>(row + j0));
+    } else {
+      v[u].x = j0 < n ? __ldg(row + j0) : 0.f;
+      v[u].y = j0 + 1 < n ? __ldg(row + j0 + 1) : 0.f;
+      v[u].z = j0 + 2 < n ? __ldg(row + j0 + 2) : 0.f;
+      v[u].w = j0 + 3 < n ? __ldg(row + j0 + 3) : 0.f;
+    }
+  }
   if (tid == 0) {
     f_min = 0xFFFFFFFFu;
     f_max = 0u;
     f_valid = 0u;
     f_over = 0u;
   }
+  for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
   __syncthreads();
+  uint32_t skey[8];
+  uint32_t sok = 0;  // bit 4 u + e: skey[4 u + e] is a sampled score of the row
   {
-    float4 v[2];
-    int jb[2];
+    uint32_t smin = 0xFFFFFFFFu, smax = 0u;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const int i = warp + kWarps * u;
-      jb[u] = i < sblk ? 128 * (i * nblk / sblk) : n;  // i * nblk < 2^16: 32-bit math
-      const int j0 = jb[u] + 4 * lane;
-      if (vec && j0 + 4 <= n) {
-        v[u] = __ldg(reinterpret_cast<const float4*>(row + j0));
-      } else {
-        v[u].x = j0 < n ? __ldg(row + j0) : 0.f;
-        v[u].y = j0 + 1 < n ? __ldg(row + j0 + 1) : 0.f;
-        v[u].z = j0 + 2 < n ? __ldg(row + j0 + 2) : 0.f;
-        v[u].w = j0 + 3 < n ? __ldg(row + j0 + 3) : 0.f;
-      }
-    }
-    uint32_t smin = 0xFFFFFFFFu, smax = 0u, svalid = 0;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int i = warp + kWarps * u;
-      if (i >= sblk) break;  // warp-uniform
+      const bool blk = warp + kWarps * u < sblk;
       const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool ok = jb[u] + 4 * lane + e < n;
+        const bool ok = blk && jb[u] + 4 * lane + e < n;
         const uint32_t key = order_key(f[e]);
-        skeys[128 * i + 4 * lane + e] = key;
+        skey[4 * u + e] = key;
+        sok |= ok ? 1u << (4 * u + e) : 0u;
         if (ok) {
           smin = min(smin, key);
           smax = max(smax, key);
-          ++svalid;
         }
       }
     }
+    uint32_t svalid = (uint32_t)__popc(sok);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       smin = min(smin, __shfl_xor_sync(0xffffffffu, smin, o));
@@ -279,7 +282,6 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
       atomicAdd(&f_valid, svalid);
     }
   }
-  for (int i = tid; i < kSelBins; i += kThreads) hist[i] = 0;
   __syncthreads();
   const uint32_t S = f_valid, lo_s = f_min, hi_s = f_max;
   // sample rank m whose key becomes tau: about 1.5 k of the row (k itself when the sample is the row)
@@ -292,10 +294,9 @@ __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool v
     const int bits = 32 - __clz(range);
     const int shift = bits > 12 ? bits - 12 : 0;
     const uint32_t nb = (range >> shift) + 1;
-    // only the last sampled block can hold slots past the row's end; they are skipped
-    const int last_valid = 128 * (sblk - 1) + (n - 128 * ((sblk - 1) * nblk / sblk));
-    for (int i = tid; i < 128 * sblk; i += kThreads)
-      if (i < last_valid) atomicAdd(&hist[(skeys[i] - lo_s) >> shift], 1u);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if ((sok >> q) & 1u) atomicAdd(&hist[(skey[q] - lo_s) >> shift], 1u);
     __syncthreads();
     uint32_t above, count;
     const uint32_t b = bin_from_top(hist, nb, m, part, sh, above, count);
