@@ -85,3 +85,23 @@ def test_sampled_threshold_rows(k):
     got = _run(s, kvlen, k)
     ref = oracle.topk(s.astype(np.float64), kvlen, k)
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("c", [1, 20, 31, 33, 500, 1000])
+def test_tie_group_at_the_threshold(c):
+    """A group of c equal scores straddles the k-th place (the rest distinct): the threshold bin of
+    the candidate histogram holds about c entries, so small groups take the one-warp ranking, larger
+    ones the block-wide sort, and the lowest indices of the group win."""
+    rng = np.random.default_rng(c)
+    ld, k = 40000, 2048
+    rows = []
+    for r in range(4):
+        s = (rng.permutation(ld) + 1).astype(np.float32)       # distinct, exactly representable
+        v = np.float32(ld - k + 1 + c // 2)                      # the group's value: c // 2 of it above place k
+        s[(s <= v) & (s > v - c)] = v
+        rows.append(s)
+    s = np.stack(rows)
+    kvlen = np.array([ld, ld, ld - 5, 30000], np.int32)
+    got = _run(s, kvlen, k)
+    ref = oracle.topk(s.astype(np.float64), kvlen, k)
+    assert np.array_equal(got, ref)
