@@ -4,9 +4,11 @@ One step = one pass of the whole hot path over one batch: hs_indexer_scores -> h
 hs_sparse_mla_fwd. The default line is the long prefill: one step is one 131,072-token sequence
 as 64 sequential chunks of 2,048 tokens (64 x 128-d FP8 index heads, top-2048, 64 MLA heads,
 paged FP8 KV), i.e. 192 launches; it also reports the per-chunk curve, the chunk where the indexer
-overtakes attention, and the MTP-decode (64 requests x (1+3) tokens, contexts 16K-64K) and
-chunked-prefill (2,048 tokens after 65,536) workloads as extra keys. Other workloads are available
-for analysis with --config 1|2|3|5, --kv-append, --kv-offload.
+overtakes attention, and the MTP-decode (64 requests x (1+3) tokens, contexts 16K-64K; indexer
+and top-k as the one call hs_indexer_topk), chunked-prefill (2,048 tokens after 65,536) and
+mixed-residency (32 requests, contexts 256K-1M with the older rows in pinned host memory; resolve
++ sparse MLA, 50 steps) workloads as extra keys. Other workloads are available for analysis with
+--config 1|2|3|5, --kv-append, --kv-offload.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 4]
 
@@ -803,6 +805,9 @@ def run_long_prefill_pass(args):
             w = build_workload(cfg, rank_seed(cfg, 0))
             others[w.name] = measure_hot_path(w, steps, 3, dev, pk, fused=cfg == 2)
             del w
+        if world == 1:  # the mixed-residency decode (its host tier is 13 GB of pinned memory per process)
+            hsp = measure_hisparse(32, 50)
+            others[hsp["workload"]] = hsp
 
     # ---- CPU baseline: the oracle on a stratified sample of the pass
     cpu = None
@@ -933,13 +938,21 @@ def run_hisparse(args):
     tokens resident, older rows in pinned host memory, 4,096 hot slots per request; 50 steps of
     resolve + sparse MLA over the Zipf(1.1) index stream with 80 % step-to-step overlap."""
     import torch
+    torch.cuda.set_device(0)
+    line = {"metric": "HiSparse decode tokens/s (resolve+attn)"}
+    line.update(measure_hisparse(args.hisparse_requests, args.hisparse_steps))
+    print(json.dumps(line), flush=True)
+
+
+def measure_hisparse(requests: int, nsteps: int) -> dict:
+    """The mixed-residency decode measured on the current device (see run_hisparse)."""
+    import torch
     import dsa_sparse_mla_gb300 as hs
     from dsa_sparse_mla_gb300 import costmodel as cm, inputs
     from dsa_sparse_mla_gb300.pipeline import DeviceHiSparse, pinned_uint8
-    torch.cuda.set_device(0)
     hs.load()
     t0 = time.perf_counter()
-    hw = inputs.config5(B=args.hisparse_requests, steps=args.hisparse_steps, host_alloc=pinned_uint8)
+    hw = inputs.config5(B=requests, steps=nsteps, host_alloc=pinned_uint8)
     gen_s = time.perf_counter() - t0
     dh = DeviceHiSparse(hw)
     stream = torch.cuda.current_stream()
@@ -981,7 +994,7 @@ def run_hisparse(args):
     warm = slice(1, steps)
     miss_bytes = cnt[:, 2].astype(np.float64) * 656
     mla_w = cm.mla_work(hw.H, hw.B * hw.k, hw.B)
-    line = {"metric": "HiSparse decode tokens/s (resolve+attn)", "workload": hw.name, "requests": hw.B,
+    line = {"workload": hw.name, "requests": hw.B,
             "steps": steps, "topk": hw.k, "hot_slots": hw.S, "mla_heads": hw.H,
             "value": round(hw.B * (steps - 1) / ((t_res[warm] + t_mla[warm]).sum() * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step_warm": round(float((t_res[warm] + t_mla[warm]).mean()), 4),
@@ -1004,7 +1017,9 @@ def run_hisparse(args):
                           "note": "hs_hisparse_touch_host once before step 0 (setup, not in value)"},
             "device_flag": hs.hs_check_flag(dh.err), "inputs_generated_s": round(gen_s, 1), "data": "synthetic",
             "l2": "no flush (consecutive decode steps)"}
-    print(json.dumps(line), flush=True)
+    del dh, hw
+    torch.cuda.empty_cache()
+    return line
 
 
 # ------------------------------------------------------------------------ reference arm -----
@@ -1067,7 +1082,8 @@ def main(argv=None):
                     help="4 (default): the long-prefill pass; 1, 2, 3: one step of that workload; 5: HiSparse decode")
     ap.add_argument("--requests", type=int, default=64, help="decode batch size (profiling runs use fewer)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="--config 4: skip the MTP-decode and chunked-prefill keys")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="--config 4: skip the MTP-decode, chunked-prefill and mixed-residency keys")
     ap.add_argument("--chunks", default="", help="--config 4: run only these chunks of the pass (comma list; profiling)")
     ap.add_argument("--no-peak", action="store_true", help="--config 4: skip the e4m3 GEMM peak measurement (profiling)")
     ap.add_argument("--reps", type=int, default=5, help="--kv-append / --kv-offload: timed launches")
