@@ -50,7 +50,7 @@ constexpr int kFastCand = kMaxCand * 2;  // fast path: candidate indices (uint32
 constexpr int kSample = 4096;          // fast path: sampled scores (at most)
 constexpr int kSmallSort = 1024;       // fast path: candidates of the threshold bin (at most)
 constexpr int kFastMaxN = 262144;      // fast path: rows of up to this many scores
-constexpr int kOffCand = 0;                            // uint64 [kMaxCand] (sample keys alias it)
+constexpr int kOffCand = 0;                            // uint64 [kMaxCand] (fast path: candidate indices)
 constexpr int kOffHist = kOffCand + kMaxCand * 8;      // uint32 [kBins]
 constexpr int kOffCKey = kOffHist + kBins * 4;         // fast path: uint32 [kFastCand] candidate scores
 constexpr int kSmem = kOffCKey + kFastCand * 4;         // (the fast path's small sort buffer sits in hist)
@@ -211,7 +211,7 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
 // Fast path (see the file header). Returns true when it wrote the row's output; false (with the
 // output untouched) when the exact path has to run. All decisions are block-uniform.
 // Candidates are score indices in per-warp regions of kFastCand / kWarps slots (the memory of the
-// exact path's candidate buffer); their keys are re-read from the row (L2) when needed.
+// exact path's candidate buffer), with their scores at the same slots of cscore.
 __device__ bool fast_topk(const float* row, int n, int k, int c0, int c1, bool vec, uint32_t* hist, uint32_t* cidx,
                           uint32_t* cscore, int32_t* out) {
   constexpr int kRegion = kFastCand / kWarps;  // candidate slots per warp
