@@ -137,6 +137,31 @@ __device__ __forceinline__ int32_t block_scan_excl(int32_t v, int32_t* part, int
   return before + incl - v;
 }
 
+// The indexer's pipeline waits sleep in the barrier (a suspend-time hint) instead of spinning: the
+// epilogue warps wait for their accumulator half of the time, and spinning warps take issue slots
+// from the warps that compute on the same sub-partition. The hint bounds each sleep; the phase's
+// completion ends it. Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)  // hint in ns
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if ((it & 7) == 7 && globaltimer() - t0 > kWaitLimitNs) {
+      flag_error(err, HS_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 template <int DI, int HI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -395,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kt = sSegLo[s2]; kt < sSegHi[s2]; ++kt, ++it_prod) {
             const int st = it_prod % kStages;
             const uint32_t ph = (uint32_t)(it_prod / kStages) & 1u;
-            if (!mbar_wait(&empty[st], ph ^ 1u, p.err)) {
+            if (!mbar_wait_sleep(&empty[st], ph ^ 1u, p.err)) {
               *abort_flag = 1;
               break;
             }
@@ -439,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph = (uint32_t)(it_mma / kStages) & 1u;
             const int bb = it_mma & 1;
             const uint32_t aph = (uint32_t)(it_mma >> 1) & 1u;
-            if (!mbar_wait(&full[st], ph, p.err) || !mbar_wait(&acc_empty[bb], aph ^ 1u, p.err)) {
+            if (!mbar_wait_sleep(&full[st], ph, p.err) || !mbar_wait_sleep(&acc_empty[bb], aph ^ 1u, p.err)) {
               ok = false;
               break;
             }
@@ -483,7 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int bb = it_epi & 1;
           if (bb != parity) continue;
           const uint32_t aph = (uint32_t)(it_epi >> 1) & 1u;
-          const bool go = !*abort_flag && warp_wait(&acc_full[bb], aph, p.err, lane);
+          int gi = 1;
+          if (lane == 0) gi = !*abort_flag && mbar_wait_sleep(&acc_full[bb], aph, p.err) ? 1 : 0;
+          const bool go = __shfl_sync(0xffffffffu, gi, 0) != 0;
           if (!__all_sync(0xffffffffu, go)) {
             *abort_flag = 1;
             ok = false;
