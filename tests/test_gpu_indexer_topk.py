@@ -86,3 +86,12 @@ def test_shared_sets_fused_step():
     assert hs_check_flag(a.err) == 0 and hs_check_flag(b.err) == 0
     assert torch.equal(a.idx, b.idx)
     assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def test_one_call_chunked_prefill():
+    """A prefill chunk through the one call (2,048 tokens after 65,536 cached, 553 MB of scores, far
+    more than L2 holds): still the two calls' indices, bit for bit."""
+    w = inputs.config3()
+    dw = DeviceWorkload.from_host(w)
+    i1, i2 = _both(dw, w.ld)
+    assert np.array_equal(i1, i2)
