@@ -333,10 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         sTokSeg[tid] = (n > 0) ? r : -1;  // request for now; turned into a segment id below
       }
       if (tid < G * HI) {
-        // folded weight w * q_scale; heads 4m+2, 4m+3 take their ReLU as x + |x| = 2 max(x, 0), so
-        // their weight carries the factor 1/2 (exact)
+        // folded weight w * q_scale; every head takes its ReLU as x + |x| = 2 max(x, 0) (packed
+        // fp32x2 adds, two heads per instruction), so the weight carries the factor 1/2 (exact)
         const int g = tid / HI, h = tid % HI, t = p.t_base + t0 + g;
-        const float half = (h & 2) ? 0.5f : 1.f;
+        const float half = 0.5f;
         sW[tid] = (t < p.T) ? half * (p.weights[(int64_t)t * HI + h] * p.q_scale[(int64_t)t * HI + h]) : 0.f;
       }
       __syncthreads();
@@ -542,8 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float x1 = __uint_as_float(acc[c / 32][c % 32 + 1]);
               const float x2 = __uint_as_float(acc[c / 32][c % 32 + 2]);
               const float x3 = __uint_as_float(acc[c / 32][c % 32 + 3]);
-              ffma2(a0, a1, fmaxf(x0, 0.f), fmaxf(x1, 0.f), wv.x, wv.y);
-              ffma2(a2, a3, x2 + fabsf(x2), x3 + fabsf(x3), wv.z, wv.w);
+              const float2 r01 = __fadd2_rn(make_float2(x0, x1), make_float2(fabsf(x0), fabsf(x1)));
+              const float2 r23 = __fadd2_rn(make_float2(x2, x3), make_float2(fabsf(x2), fabsf(x3)));
+              ffma2(a0, a1, r01.x, r01.y, wv.x, wv.y);
+              ffma2(a2, a3, r23.x, r23.y, wv.z, wv.w);
             });
             return (a0 + a1) + (a2 + a3);
           };
