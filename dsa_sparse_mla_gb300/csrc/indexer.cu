@@ -499,15 +499,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t wsl = smem_u32(sW + col0);  // this warp's folded weights
       float* const srow = p.scores + (int64_t)(p.t_base + t0 + g0) * p.ld + row;  // used only where lim > 0
       bool ok = true;
+      const bool keep = p.keep_scores != 0;
+      const uint64_t pol_last = l2_policy_evict_last();
       for (int s2 = 0; s2 < nseg && ok; ++s2) {
         const int lo = sSegLo[s2], hi = sSegHi[s2];
         const int jn = sSegN[s2];                                     // keys of the segment's longest token
         const int32_t* blk_s = sBlk + sSegPg[s2] - 2 * lo;           // page of (tile kt, half) at 2 kt + half
         const int32_t* lim_s = sLim + s2 * kMaxG + g0;
-        for (int kt = lo; kt < hi; ++kt, ++it_epi) {
-          const int bb = it_epi & 1;
-          if (bb != parity) continue;
-          const uint32_t aph = (uint32_t)(it_epi >> 1) & 1u;
+        // only the tiles of this warp's parity: tile kt has the running tile number ie
+        const int ie0 = it_epi - lo;
+        it_epi += hi - lo;
+        for (int kt = lo + ((parity - (ie0 + lo)) & 1); kt < hi; kt += 2) {
+          const uint32_t ie = (uint32_t)(ie0 + kt);
+          const int bb = parity;
+          const uint32_t aph = (ie >> 1) & 1u;
           int gi = 1;
           if (lane == 0) gi = !*abort_flag && mbar_wait_sleep(&acc_full[bb], aph, p.err) ? 1 : 0;
           const bool go = __shfl_sync(0xffffffffu, gi, 0) != 0;
@@ -528,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j < jn) {
             const int32_t blk = blk_s[2 * kt + (row >> 6)];
             if (blk >= 0)
-              ks = p.scale_tma ? sScale[(it_epi % kScaleRing) * kBlockM + row]
+              ks = p.scale_tma ? sScale[(ie % kScaleRing) * kBlockM + row]
                                : __ldg(p.k_scale + (int64_t)blk * 64 + (j & 63));
           }
           auto token_score = [&](auto cc, auto kc) -> float {  // weighted ReLU sum of token kc of chunk cc
@@ -568,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int g = c2 * kTok + k;
                 if (j < lim_s[g]) {
                   float* dst = srow + (int64_t)g * p.ld + (int64_t)kt * kBlockM;
-                  if (p.keep_scores) st_global_hint(dst, ks * sc[c2][k], l2_policy_evict_last());
+                  if (keep) st_global_hint(dst, ks * sc[c2][k], pol_last);
                   else *dst = ks * sc[c2][k];
                 }
               }
